@@ -1,0 +1,323 @@
+/*
+ * Double-precision CPU oracle for the fused hard-label cross-entropy and the
+ * row-wise softmax forward/backward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file; only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * Every function is the plain textbook definition, written out row by row in
+ * double precision, with no blocking, fusion or online recurrence:
+ *
+ *   m   = max_i x_i
+ *   Z   = sum_i exp(x_i - m)                (compensated sum, index order)
+ *   p_i = exp(x_i - m) / Z
+ *   l_r = m + ln Z - x_y                    (= -ln p_y)
+ *   g_i = (p_i - [i == y]) / n              (n = number of non-ignored rows)
+ *   L   = (sum over non-ignored rows of l_r) / n
+ *
+ * Sources, by page and section:
+ *   - Liger-Kernel, src/liger_kernel/ops/cross_entropy.py,
+ *     liger_cross_entropy_kernel docstring: hard labels with mean reduction,
+ *     following PyTorch's CrossEntropyLoss.
+ *   - same kernel, steps 1-2: a row whose target equals ignore_index gets an
+ *     all-zero gradient and contributes no loss.
+ *   - same kernel, step 4 comment: dx_i = softmax(x_i)/N for i != y and
+ *     dx_y = (softmax(x_y) - 1)/N, N = number of non-ignored rows in the batch.
+ *   - same kernel, step 5 comment: loss = -(x_y - max(x) - log sum e^(x-max)).
+ *   - LigerCrossEntropyFunction.forward: n_non_ignore counts targets that
+ *     differ from ignore_index over the whole batch; the loss is the sum of the
+ *     per-row losses divided by it.
+ *   - "python sum function examples (triton.language)", _softmax and
+ *     softmax_kernel: y = exp(x - max x) / sum exp(x - max x) per row.
+ *   - same page, _backward (block-sparse softmax backward), dense math with
+ *     scale 1: dx = y * (dy - sum(y * dy)).
+ *
+ * Readings where the pages are silent:
+ *   - n == 0 (every row ignored): the mean is 0/0 = NaN and every gradient row
+ *     is zero, as each row takes the ignore exit.
+ *   - a target outside [0, V) that is not ignore_index: the row's loss is NaN,
+ *     its gradient row is the unmodified input, and the row is counted as bad.
+ *     Such a row still counts toward n (n counts targets != ignore_index).
+ *   - bf16 inputs are widened exactly to double before any arithmetic.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* Read element idx of a row stored as fp32 or as raw bf16 bits, widened
+ * exactly to double. */
+static double load_elem(const void *base, int dtype, int64_t idx)
+{
+    if (dtype == ORACLE_F32)
+        return (double)((const float *)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Neumaier's compensated summation (Neumaier 1974), summed in index order. */
+typedef struct {
+    double s, c;
+} csum_t;
+
+static void csum_add(csum_t *a, double v)
+{
+    double t = a->s + v;
+    if (fabs(a->s) >= fabs(v))
+        a->c += (a->s - t) + v;
+    else
+        a->c += (v - t) + a->s;
+    a->s = t;
+}
+
+static double csum_value(const csum_t *a) { return a->s + a->c; }
+
+int oracle_ce_count(const int64_t *targets, int64_t M, int64_t V, int64_t ignore_index,
+                    int64_t *n_out, int64_t *bad_out)
+{
+    int64_t n = 0, bad = 0;
+    for (int64_t r = 0; r < M; ++r) {
+        int64_t y = targets[r];
+        if (y == ignore_index)
+            continue;
+        ++n;
+        if (y < 0 || y >= V)
+            ++bad;
+    }
+    if (n_out)
+        *n_out = n;
+    if (bad_out)
+        *bad_out = bad;
+    return 0;
+}
+
+/* One cross-entropy row.  x: the row's first element; grad: V doubles or NULL. */
+static void ce_row(const void *x, int dtype, int64_t V, int64_t y, int64_t ignore_index,
+                   int64_t n, double *grad, double *loss)
+{
+    if (y == ignore_index) {
+        if (grad)
+            for (int64_t i = 0; i < V; ++i)
+                grad[i] = 0.0;
+        *loss = 0.0;
+        return;
+    }
+    if (y < 0 || y >= V) {
+        if (grad)
+            for (int64_t i = 0; i < V; ++i)
+                grad[i] = load_elem(x, dtype, i);
+        *loss = NAN;
+        return;
+    }
+    /* pass 1: the maximum */
+    double m = -INFINITY;
+    for (int64_t i = 0; i < V; ++i) {
+        double v = load_elem(x, dtype, i);
+        if (v > m)
+            m = v;
+    }
+    /* pass 2: the normaliser */
+    csum_t z = {0.0, 0.0};
+    for (int64_t i = 0; i < V; ++i)
+        csum_add(&z, exp(load_elem(x, dtype, i) - m));
+    double Z = csum_value(&z);
+    /* the row loss, -ln p_y */
+    *loss = m + log(Z) - load_elem(x, dtype, y);
+    /* pass 3: the gradient */
+    if (grad) {
+        for (int64_t i = 0; i < V; ++i) {
+            double p = exp(load_elem(x, dtype, i) - m) / Z;
+            double onehot = (i == y) ? 1.0 : 0.0;
+            grad[i] = (p - onehot) / (double)n;
+        }
+    }
+}
+
+static void softmax_fwd_row(const void *x, int dtype, int64_t N, double *y)
+{
+    double m = -INFINITY;
+    for (int64_t i = 0; i < N; ++i) {
+        double v = load_elem(x, dtype, i);
+        if (v > m)
+            m = v;
+    }
+    csum_t z = {0.0, 0.0};
+    for (int64_t i = 0; i < N; ++i)
+        csum_add(&z, exp(load_elem(x, dtype, i) - m));
+    double Z = csum_value(&z);
+    for (int64_t i = 0; i < N; ++i)
+        y[i] = exp(load_elem(x, dtype, i) - m) / Z;
+}
+
+static void softmax_bwd_row(const void *y, const void *dy, int dtype, int64_t N, double *dx)
+{
+    csum_t s = {0.0, 0.0};
+    for (int64_t i = 0; i < N; ++i)
+        csum_add(&s, load_elem(y, dtype, i) * load_elem(dy, dtype, i));
+    double S = csum_value(&s);
+    for (int64_t i = 0; i < N; ++i)
+        dx[i] = load_elem(y, dtype, i) * (load_elem(dy, dtype, i) - S);
+}
+
+/* ---- a plain parallel-for over the requested rows (rows are independent) ---- */
+
+enum { JOB_CE = 0, JOB_SM_FWD = 1, JOB_SM_BWD = 2 };
+
+typedef struct {
+    int kind, dtype;
+    const void *a;     /* logits, x, or y */
+    int64_t a_stride;
+    const void *b;     /* dy for the softmax backward */
+    int64_t b_stride;
+    const int64_t *targets;
+    int64_t ncols, ignore_index, n;
+    const int64_t *rows; /* NULL: rows 0..nrows-1 */
+    int64_t nrows;
+    double *out;       /* nrows x ncols, or NULL (cross-entropy only) */
+    double *row_loss;  /* nrows (cross-entropy only) */
+    int64_t begin, end;
+} job_t;
+
+static size_t elem_size(int dtype) { return dtype == ORACLE_F32 ? 4 : 2; }
+
+static void *run_job(void *arg)
+{
+    job_t *j = (job_t *)arg;
+    size_t es = elem_size(j->dtype);
+    for (int64_t k = j->begin; k < j->end; ++k) {
+        int64_t r = j->rows ? j->rows[k] : k;
+        const char *ra = (const char *)j->a + (size_t)r * (size_t)j->a_stride * es;
+        double *o = j->out ? j->out + (size_t)k * (size_t)j->ncols : NULL;
+        if (j->kind == JOB_CE) {
+            ce_row(ra, j->dtype, j->ncols, j->targets[r], j->ignore_index, j->n, o,
+                   &j->row_loss[k]);
+        } else if (j->kind == JOB_SM_FWD) {
+            softmax_fwd_row(ra, j->dtype, j->ncols, o);
+        } else {
+            const char *rb = (const char *)j->b + (size_t)r * (size_t)j->b_stride * es;
+            softmax_bwd_row(ra, rb, j->dtype, j->ncols, o);
+        }
+    }
+    return NULL;
+}
+
+static int run_parallel(const job_t *proto, int nthreads)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    if ((int64_t)nthreads > proto->nrows)
+        nthreads = proto->nrows > 0 ? (int)proto->nrows : 1;
+    job_t jobs[256];
+    pthread_t tids[256];
+    int64_t per = (proto->nrows + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *proto;
+        jobs[t].begin = (int64_t)t * per;
+        jobs[t].end = jobs[t].begin + per < proto->nrows ? jobs[t].begin + per : proto->nrows;
+        if (jobs[t].begin > jobs[t].end)
+            jobs[t].begin = jobs[t].end;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, run_job, &jobs[t]) != 0) {
+            /* run the remaining ranges on this thread instead */
+            for (int u = t; u < nthreads; ++u)
+                run_job(&jobs[u]);
+            break;
+        }
+        started = t;
+    }
+    run_job(&jobs[0]);
+    for (int t = 1; t <= started; ++t)
+        pthread_join(tids[t], NULL);
+    return 0;
+}
+
+/* Cross-entropy rows.  rows[k] (or k when rows is NULL) names the input row;
+ * grad (nrows x V doubles, or NULL) and row_loss (nrows doubles) are indexed by
+ * k.  n is the batch-wide non-ignored count from oracle_ce_count. */
+int oracle_ce_rows(const void *logits, int dtype, int64_t stride, const int64_t *targets,
+                   int64_t V, int64_t ignore_index, int64_t n, const int64_t *rows,
+                   int64_t nrows, double *grad, double *row_loss, int nthreads)
+{
+    if (!logits || !targets || !row_loss || V < 1 || stride < V || nrows < 0)
+        return 1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+        return 1;
+    job_t j;
+    memset(&j, 0, sizeof j);
+    j.kind = JOB_CE;
+    j.dtype = dtype;
+    j.a = logits;
+    j.a_stride = stride;
+    j.targets = targets;
+    j.ncols = V;
+    j.ignore_index = ignore_index;
+    j.n = n;
+    j.rows = rows;
+    j.nrows = nrows;
+    j.out = grad;
+    j.row_loss = row_loss;
+    return run_parallel(&j, nthreads);
+}
+
+/* L = sum_r row_loss[r] / n over all M rows (ignored rows hold 0). */
+double oracle_ce_mean(const double *row_loss, int64_t M, int64_t n)
+{
+    csum_t s = {0.0, 0.0};
+    for (int64_t r = 0; r < M; ++r)
+        csum_add(&s, row_loss[r]);
+    return csum_value(&s) / (double)n;
+}
+
+int oracle_softmax_fwd_rows(const void *x, int dtype, int64_t stride, int64_t N,
+                            const int64_t *rows, int64_t nrows, double *y, int nthreads)
+{
+    if (!x || !y || N < 1 || stride < N || nrows < 0)
+        return 1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+        return 1;
+    job_t j;
+    memset(&j, 0, sizeof j);
+    j.kind = JOB_SM_FWD;
+    j.dtype = dtype;
+    j.a = x;
+    j.a_stride = stride;
+    j.ncols = N;
+    j.rows = rows;
+    j.nrows = nrows;
+    j.out = y;
+    return run_parallel(&j, nthreads);
+}
+
+int oracle_softmax_bwd_rows(const void *y, int64_t y_stride, const void *dy, int64_t dy_stride,
+                            int dtype, int64_t N, const int64_t *rows, int64_t nrows, double *dx,
+                            int nthreads)
+{
+    if (!y || !dy || !dx || N < 1 || y_stride < N || dy_stride < N || nrows < 0)
+        return 1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+        return 1;
+    job_t j;
+    memset(&j, 0, sizeof j);
+    j.kind = JOB_SM_BWD;
+    j.dtype = dtype;
+    j.a = y;
+    j.a_stride = y_stride;
+    j.b = dy;
+    j.b_stride = dy_stride;
+    j.ncols = N;
+    j.rows = rows;
+    j.nrows = nrows;
+    j.out = dx;
+    return run_parallel(&j, nthreads);
+}
