@@ -1,0 +1,432 @@
+"""Benchmark of the fused cross-entropy hot path (and the row softmax) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gbce|reference]
+
+One step is one ``ce_fwd_bwd`` call (target load, ignore test, non-ignored
+count, online normaliser, in-place gradient, row losses, mean) over the
+whole batch of the workload, inputs resident in HBM.  The call overwrites its
+input, so before every step the pristine logits are copied back and L2 is
+flushed, outside the timed span; each step is timed alone with CUDA events
+between a barrier + synchronize on both sides.  Rank 0 prints one JSON line.
+
+With N > 1 (torchrun) every rank runs its own replica of the workload on its
+own GPU (rows are independent; there is no collective on the data path) and
+the value is the rows of all ranks over the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (double precision, all host cores)
+on a bounded sample of the same workload per step instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "fused CE fwd+bwd rows/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+DEFAULT_WORKLOAD = "ce_bf16_16384x128256"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = [os.path.join(ROOT, "cross_entropy_loss_ce_gb300", "csrc", f)
+                  for f in ("row_kernels.cuh", "device.cuh")]
+
+
+# ---------------------------------------------------------------------------
+# helpers
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def esize(dtype):
+    return 4 if dtype == torch.float32 else 2
+
+
+def ce_algorithmic_bytes(w, targets_host: np.ndarray) -> int:
+    """Bytes the method must move per launch of the row kernel: every live row
+    read once and written once, every ignored row written once, plus per row
+    the int64 target read and the fp32 row loss written."""
+    ignored = int((targets_host == workloads.IGNORE_INDEX).sum())
+    live = w.M - ignored
+    row = w.V * esize(w.dtype)
+    return live * 2 * row + ignored * row + w.M * (8 + 4)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the row kernel from the committed ncu summary,
+    or None when there is none or the kernel source changed since."""
+    path = os.path.join(PROFILE_DIR, f"ce_rows_{workload}.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = re.search(r"kernel_source_sha256_16:\s*(\w+)", text)
+    val = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not src or not val or src.group(1) != kernel_source_hash():
+        return None
+    return float(val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def barrier_sync(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on this host's cores
+
+def oracle_rows_per_s(w, x_host: torch.Tensor, t_host: torch.Tensor, block: int = 512):
+    """Time the oracle (loss + full gradient) over the rows of x_host, in blocks."""
+    import oracle
+    V = w.V
+    xa = oracle.host_array(x_host)
+    ta = t_host.numpy()
+    n, _ = oracle.ce_count(ta, V)
+    nthreads = oracle.default_threads()
+    t0 = time.perf_counter()
+    for b0 in range(0, xa.shape[0], block):
+        rows = np.arange(b0, min(b0 + block, xa.shape[0]))
+        oracle.ce_rows(xa, ta, V, n, rows=rows, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return xa.shape[0] / dt, dt, nthreads
+
+
+def run_reference(args, ws, rank):
+    """--impl reference: the oracle on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return
+    w = workloads.CE_WORKLOADS[args.workload]
+    sample = args.ref_rows
+    ws_ = w.with_rows(sample)
+    x, t = workloads.make_ce_inputs(ws_, "cpu")
+    for _ in range(args.warmup):
+        oracle_rows_per_s(w, x, t)
+    times = []
+    threads = 1
+    for _ in range(args.steps):
+        _, dt, threads = oracle_rows_per_s(w, x, t)
+        times.append(dt)
+    total = float(np.sum(times))
+    value = sample * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "V": w.V, "logits_dtype": str(w.dtype),
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{sample} rows of {w.name} per step (seeded CPU draw), "
+                                   f"loss and full gradient in double precision"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+
+def flush_l2(buf: torch.Tensor):
+    buf.add_(1)  # read + write every line of a buffer larger than L2
+
+
+def time_ce(w, xd0, td, steps, warmup, ws, flush):
+    """Per-step CUDA-event time of ce_fwd_bwd on restored inputs; (total ms, kernel ms, launches)."""
+    import cross_entropy_loss_ce_gb300 as gbce
+    xd = torch.empty_like(xd0)
+    loss = torch.empty((), dtype=torch.float32, device="cuda")
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(warmup):
+        xd.copy_(xd0)
+        gbce.ce_fwd_bwd(xd, td, workloads.IGNORE_INDEX, loss)
+    torch.cuda.synchronize()
+    if gbce.last_error() != gbce.OK:
+        raise RuntimeError("device error flag raised during warm-up")
+    gbce.timing_read()
+    gbce.timing_enable(True)
+    total = 0.0
+    for _ in range(steps):
+        xd.copy_(xd0)
+        flush_l2(flush)
+        barrier_sync(ws)
+        start.record()
+        gbce.ce_fwd_bwd(xd, td, workloads.IGNORE_INDEX, loss)
+        stop.record()
+        barrier_sync(ws)
+        total += start.elapsed_time(stop)
+    kms, launches = gbce.timing_read()
+    gbce.timing_enable(False)
+    if gbce.last_error() != gbce.OK:
+        raise RuntimeError("device error flag raised during the timed steps")
+    return total, kms, launches, float(loss.item())
+
+
+def time_ce_e2e(w, x_pinned, t_pinned, steps, ws):
+    """End to end through the public call: pinned host -> device copy of the
+    step's logits and targets, the call, device -> host read of the loss."""
+    import cross_entropy_loss_ce_gb300 as gbce
+    xd = torch.empty(x_pinned.shape, dtype=x_pinned.dtype, device="cuda")
+    td = torch.empty(t_pinned.shape, dtype=t_pinned.dtype, device="cuda")
+    loss = torch.empty((), dtype=torch.float32, device="cuda")
+    loss_host = torch.empty((), dtype=torch.float32).pin_memory()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total = 0.0
+    for i in range(steps + 1):
+        barrier_sync(ws)
+        start.record()
+        xd.copy_(x_pinned, non_blocking=True)
+        td.copy_(t_pinned, non_blocking=True)
+        gbce.ce_fwd_bwd(xd, td, workloads.IGNORE_INDEX, loss)
+        loss_host.copy_(loss, non_blocking=True)
+        stop.record()
+        barrier_sync(ws)
+        if i > 0:  # the first iteration is a warm-up
+            total += start.elapsed_time(stop)
+    h2d = x_pinned.numel() * x_pinned.element_size() + t_pinned.numel() * 8
+    return total, h2d, 4
+
+
+def time_softmax(steps, warmup, ws, flush, N=16384):
+    """Softmax forward + backward on the 4096 x N fp32 workload (per-call events)."""
+    import cross_entropy_loss_ce_gb300 as gbce
+    M = workloads.SOFTMAX_M
+    x, y, dy = workloads.make_softmax_inputs(M, N, device="cuda")
+    out = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for _ in range(warmup):
+        gbce.softmax_fwd(x, out)
+        gbce.softmax_bwd(y, dy, dx)
+    fwd = bwd = 0.0
+    for _ in range(steps):
+        flush_l2(flush)
+        barrier_sync(ws)
+        ev[0].record()
+        gbce.softmax_fwd(x, out)
+        ev[1].record()
+        flush_l2(flush)
+        ev[2].record()
+        gbce.softmax_bwd(y, dy, dx)
+        stop = torch.cuda.Event(enable_timing=True)
+        stop.record()
+        barrier_sync(ws)
+        fwd += ev[0].elapsed_time(ev[1])
+        bwd += ev[2].elapsed_time(stop)
+    return fwd / steps, bwd / steps, M, N
+
+
+def run_gbce(args, ws, rank, local):
+    import cross_entropy_loss_ce_gb300 as gbce
+    gbce.load_library()
+    torch.cuda.set_device(local)
+    w = workloads.CE_WORKLOADS[args.workload]
+    xd0, td = workloads.make_ce_inputs(w, "cuda")
+    t_host = td.cpu().numpy()
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    peak, peak_kind = measured_peaks()
+
+    with ClockSampler(local) as clocks:
+        total_ms, kernel_ms, launches, loss_val = time_ce(w, xd0, td, args.steps, args.warmup,
+                                                          ws, flush)
+    clk = clocks.summary()
+    total_ms = max_over_ranks(total_ms, ws)
+    rows_all = sum_over_ranks(float(w.M * args.steps), ws)
+    value = rows_all / (total_ms / 1e3)
+    ms_per_step = total_ms / args.steps
+    alg = ce_algorithmic_bytes(w, t_host)
+    kavg_ms = kernel_ms / max(launches, 1)
+    achieved = alg / (kavg_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                "kernel": "rows_resident_kernel<CE>", "kernel_ms": kavg_ms,
+                "algorithmic_bytes": alg, "peak_kind": f"{peak_kind} (hbm_gbs, burst)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "V": w.V, "ignore_frac": w.ignore_frac,
+                   "logits": f"N(0,{w.std}^2)" + (f" + {w.spike} spike/row" if w.spike else ""),
+                   "l2": "inputs (4.2 GB) larger than L2, and a 512 MB L2 flush before each step",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "step_hbm_gbs": alg / (ms_per_step / 1e3) / 1e9,
+        "loss": loss_val,
+        "roofline": roofline,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+
+    if not args.no_softmax:
+        fwd_ms, bwd_ms, M, N = time_softmax(max(args.steps // 2, 5), args.warmup, ws, flush)
+        fwd_b, bwd_b = 2 * M * N * 4, 3 * M * N * 4
+        line["softmax"] = {
+            "workload": f"softmax_f32_{M}x{N}", "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_rows_per_s": M / (fwd_ms / 1e3), "bwd_rows_per_s": M / (bwd_ms / 1e3),
+            "fwd_gbs": fwd_b / (fwd_ms / 1e3) / 1e9, "bwd_gbs": bwd_b / (bwd_ms / 1e3) / 1e9,
+            "fwd_frac": fwd_b / (fwd_ms / 1e3) / 1e9 / peak,
+            "bwd_frac": bwd_b / (bwd_ms / 1e3) / 1e9 / peak}
+
+    if not args.no_e2e:
+        x_pinned = xd0.cpu().pin_memory()
+        t_pinned = td.cpu().pin_memory()
+        e2e_ms, h2d, d2h = time_ce_e2e(w, x_pinned, t_pinned, min(args.steps, 10), ws)
+        e2e_ms = max_over_ranks(e2e_ms, ws)
+        e2e_steps = min(args.steps, 10)
+        line["e2e"] = {"value": sum_over_ranks(float(w.M * e2e_steps), ws) / (e2e_ms / 1e3),
+                       "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e2e_ms / e2e_steps}
+        del x_pinned
+
+    if rank == 0 and not args.no_cpu_baseline:
+        sample = min(args.cpu_rows, w.M)
+        x_host = xd0[:sample].cpu()
+        rps, dt, cores = oracle_rows_per_s(w, x_host, td[:sample].cpu())
+        line["cpu_baseline"] = {"value": rps, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                                "sample": f"first {sample} rows of {w.name}: loss and full "
+                                          f"gradient in double precision, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gbce", "reference"], default="gbce")
+    ap.add_argument("--workload", choices=list(workloads.CE_WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-rows", type=int, default=4096)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-softmax", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ws, rank, local = dist_info()
+    if ws > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank)
+        else:
+            run_gbce(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,150 @@
+"""Fused hard-label cross-entropy and row softmax on GB300 (sm_103a).
+
+Thin ctypes binding of ``_lib/libgbce.so`` (C ABI in ``include/gbce.h``): it
+checks tensor shapes, takes raw device pointers, row strides and the current
+CUDA stream from torch, and calls the library.  Every step of the computation
+runs in the library's own CUDA kernels; there is no CPU or PyTorch fallback.
+Loading fails loudly when the library has not been built
+(``python -m cross_entropy_loss_ce_gb300.build``).
+"""
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libgbce.so")
+
+GBCE_F32, GBCE_BF16 = 0, 1
+DTYPES = {torch.float32: GBCE_F32, torch.bfloat16: GBCE_BF16}
+
+OK, ERR_NULL, ERR_SIZE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA, ERR_BAD_TARGET, ERR_TIMEOUT, \
+    ERR_NO_DEVICE = range(9)
+
+_lib = None
+
+
+class GbceError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: gbce status {code}: {status_string(code)}")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgbce.so once (raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m cross_entropy_loss_ce_gb300.build`")
+        lib = ctypes.CDLL(path)
+        i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        lib.ce_fwd_bwd.argtypes = [p, i64, p, p, i64, i64, i64, ci, p]
+        lib.softmax_fwd.argtypes = [p, i64, p, i64, i64, i64, ci, p]
+        lib.softmax_bwd.argtypes = [p, i64, p, i64, p, i64, i64, i64, ci, p]
+        lib.gbce_last_error.argtypes = [p]
+        lib.gbce_status_string.argtypes = [ci]
+        lib.gbce_status_string.restype = ctypes.c_char_p
+        lib.gbce_timing_enable.argtypes = [ci]
+        lib.gbce_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                         ctypes.POINTER(ctypes.c_int64)]
+        for f in ("ce_fwd_bwd", "softmax_fwd", "softmax_bwd", "gbce_last_error",
+                  "gbce_timing_enable", "gbce_timing_read"):
+            getattr(lib, f).restype = ci
+        _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load_library().gbce_status_string(code).decode()
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _matrix(t: torch.Tensor, name: str):
+    """(pointer, row stride in elements, rows, cols) of a 2-D CUDA fp32/bf16 tensor."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in DTYPES:
+        raise TypeError(f"{name} must be float32 or bfloat16, not {t.dtype}")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} needs unit column stride")
+    stride = t.stride(0) if t.shape[0] > 1 else t.shape[1]
+    return t.data_ptr(), max(stride, t.shape[1]), t.shape[0], t.shape[1]
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise GbceError(rc, where)
+
+
+def ce_fwd_bwd(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+               loss: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Mean cross-entropy of ``logits`` [M, V] against int64 ``targets`` [M].
+
+    ``logits`` is overwritten in place with d(loss)/d(logits).  Returns a
+    0-dim float32 CUDA tensor (``loss`` when given); nothing is synchronised.
+    """
+    lp, stride, M, V = _matrix(logits, "logits")
+    if targets.dtype != torch.int64 or targets.dim() != 1 or targets.shape[0] != M:
+        raise ValueError("targets must be int64 of shape [M]")
+    if M and (not targets.is_cuda or not targets.is_contiguous()):
+        raise ValueError("targets must be a contiguous CUDA tensor")
+    if loss is None:
+        loss = torch.empty((), dtype=torch.float32, device=logits.device)
+    elif loss.dtype != torch.float32 or loss.numel() != 1 or not loss.is_cuda:
+        raise ValueError("loss must be a one-element float32 CUDA tensor")
+    rc = load_library().ce_fwd_bwd(lp, stride, targets.data_ptr(), loss.data_ptr(), M, V,
+                                   int(ignore_index), DTYPES[logits.dtype],
+                                   _stream_handle(stream))
+    _check(rc, "ce_fwd_bwd")
+    return loss
+
+
+def softmax_fwd(x: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Row softmax of ``x`` [M, N] into ``y`` (allocated when None; may be ``x``)."""
+    if y is None:
+        y = torch.empty_like(x, memory_format=torch.contiguous_format)
+    xp, xs, M, N = _matrix(x, "x")
+    yp, ys, My, Ny = _matrix(y, "y")
+    if (My, Ny) != (M, N) or y.dtype != x.dtype:
+        raise ValueError("y must match x in shape and dtype")
+    rc = load_library().softmax_fwd(xp, xs, yp, ys, M, N, DTYPES[x.dtype], _stream_handle(stream))
+    _check(rc, "softmax_fwd")
+    return y
+
+
+def softmax_bwd(y: torch.Tensor, dy: torch.Tensor, dx: torch.Tensor = None,
+                stream=None) -> torch.Tensor:
+    """dx = y * (dy - sum(y * dy, row)) for [M, N] operands (dx may be ``dy``)."""
+    if dx is None:
+        dx = torch.empty_like(dy, memory_format=torch.contiguous_format)
+    yp, ys, M, N = _matrix(y, "y")
+    dp, ds, Md, Nd = _matrix(dy, "dy")
+    xp, xs, Mx, Nx = _matrix(dx, "dx")
+    if (Md, Nd) != (M, N) or (Mx, Nx) != (M, N) or not (y.dtype == dy.dtype == dx.dtype):
+        raise ValueError("y, dy and dx must share shape and dtype")
+    rc = load_library().softmax_bwd(yp, ys, dp, ds, xp, xs, M, N, DTYPES[y.dtype],
+                                    _stream_handle(stream))
+    _check(rc, "softmax_bwd")
+    return dx
+
+
+def last_error(stream=None) -> int:
+    """Synchronise the stream and read-and-clear the device error flags."""
+    return load_library().gbce_last_error(_stream_handle(stream))
+
+
+def timing_enable(on: bool = True):
+    _check(load_library().gbce_timing_enable(1 if on else 0), "gbce_timing_enable")
+
+
+def timing_read():
+    """(summed row-kernel milliseconds, bracketed launches) since the last read."""
+    ms, n = ctypes.c_double(), ctypes.c_int64()
+    _check(load_library().gbce_timing_read(ctypes.byref(ms), ctypes.byref(n)), "gbce_timing_read")
+    return ms.value, n.value

@@ -1,0 +1,475 @@
+// C ABI of the library (declared in include/gbce.h): argument validation, the
+// launch plan chosen from the row length, stream-ordered scratch, the sticky
+// device error flags and the optional kernel-timing events.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gbce.h"
+#include "row_kernels.cuh"
+
+namespace gbce {
+
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kSliceTarget = 64 * 1024;   // staged bytes per CTA: three CTAs per SM
+constexpr int64_t kSliceMax = 200 * 1024;     // largest slice staged in shared memory
+constexpr int kMaxCluster = 16;
+
+size_t elem_size(int dtype) { return dtype == GBCE_F32 ? 4 : 2; }
+
+// ---------------------------------------------------------------------------
+// launch plan
+
+struct Plan {
+    bool resident;  // slices staged in shared memory (else the streaming fallback)
+    int C;          // CTAs per row = cluster size
+    int nt;         // threads per CTA
+    int per_vec;    // 16-byte vectors per slice
+    int chunk_vec;  // vectors per bulk copy
+    size_t smem;    // dynamic shared memory per CTA
+};
+
+int threads_for(int64_t per_vec)
+{
+    return per_vec >= 2048 ? 512 : (per_vec >= 512 ? 256 : 128);
+}
+
+// cols elements of esize bytes per operand, nbuf operands staged per row;
+// `aligned`: all operands of every row share their address modulo 16 bytes.
+Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned)
+{
+    Plan p{};
+    const int64_t nvec = cols * static_cast<int64_t>(esize) / 16;  // >= whole vectors of any row
+    int C = 1;
+    int64_t per = nvec;
+    while (C < kMaxCluster && per * 16 * nbuf > kSliceTarget) {
+        C *= 2;
+        per = (nvec + C - 1) / C;
+    }
+    if (per < 1)
+        per = 1;
+    p.C = C;
+    p.resident = aligned && per * 16 * nbuf <= kSliceMax;
+    if (!p.resident) {
+        // streaming fallback: enough CTAs that each streams ~64 KB of a row
+        int64_t bytes = cols * static_cast<int64_t>(esize);
+        int Cs = 1;
+        while (Cs < kMaxCluster && bytes / Cs > kSliceTarget)
+            Cs *= 2;
+        p.C = Cs;
+        p.nt = 512;
+        p.per_vec = 0;
+        p.chunk_vec = 0;
+        p.smem = 0;
+        return p;
+    }
+    p.per_vec = static_cast<int>(per);
+    p.nt = threads_for(per);
+    int64_t chunk = (per + kMaxChunks - 1) / kMaxChunks;
+    chunk = (chunk + p.nt - 1) / p.nt * p.nt;
+    p.chunk_vec = static_cast<int>(chunk);
+    p.smem = static_cast<size_t>(per) * 16 * nbuf;
+    return p;
+}
+
+// ---------------------------------------------------------------------------
+// kernel selection
+
+using KernelFn = void (*)(const RowArgs);
+
+template <Op OP, typename T>
+KernelFn pick_kernel(bool resident, int nt)
+{
+    if (resident) {
+        switch (nt) {
+        case 128: return rows_resident_kernel<OP, T, 128>;
+        case 256: return rows_resident_kernel<OP, T, 256>;
+        default: return rows_resident_kernel<OP, T, 512>;
+        }
+    }
+    return rows_streaming_kernel<OP, T, 512>;
+}
+
+template <Op OP>
+KernelFn pick(int dtype, bool resident, int nt)
+{
+    return dtype == GBCE_F32 ? pick_kernel<OP, float>(resident, nt)
+                             : pick_kernel<OP, __nv_bfloat16>(resident, nt);
+}
+
+// Per-device one-time function attributes (large dynamic shared memory,
+// cluster sizes above the portable 8).
+struct FnConfig {
+    KernelFn fn;
+    int device;
+};
+std::mutex g_cfg_mu;
+std::vector<FnConfig> g_cfg;
+
+cudaError_t configure(KernelFn fn, int device)
+{
+    std::lock_guard<std::mutex> lk(g_cfg_mu);
+    for (const FnConfig &c : g_cfg)
+        if (c.fn == fn && c.device == device)
+            return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSliceMax));
+    if (e != cudaSuccess)
+        return e;
+    e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess)
+        return e;
+    g_cfg.push_back({fn, device});
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// stream-ordered scratch from a library-owned pool per device (kept warm)
+
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+cudaError_t pool_for(int device, cudaMemPool_t *out)
+{
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (!g_pool[device]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = device;
+        cudaMemPool_t pool;
+        cudaError_t e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess)
+            return e;
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        g_pool[device] = pool;
+    }
+    *out = g_pool[device];
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// kernel timing (benchmarks)
+
+std::atomic<int> g_timing_on{0};
+std::mutex g_timing_mu;
+std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_timing_pending;
+std::vector<cudaEvent_t> g_event_free;
+
+cudaEvent_t take_event()
+{
+    if (!g_event_free.empty()) {
+        cudaEvent_t e = g_event_free.back();
+        g_event_free.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+struct TimedRegion {
+    cudaEvent_t start = nullptr, stop = nullptr;
+    cudaStream_t stream;
+    explicit TimedRegion(cudaStream_t s) : stream(s)
+    {
+        if (g_timing_on.load(std::memory_order_relaxed)) {
+            std::lock_guard<std::mutex> lk(g_timing_mu);
+            start = take_event();
+            stop = take_event();
+            cudaEventRecord(start, stream);
+        }
+    }
+    ~TimedRegion()
+    {
+        if (start) {
+            cudaEventRecord(stop, stream);
+            std::lock_guard<std::mutex> lk(g_timing_mu);
+            g_timing_pending.emplace_back(start, stop);
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+
+int map_error(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return GBCE_OK;
+    if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver)
+        return GBCE_ERR_NO_DEVICE;
+    return GBCE_ERR_CUDA;
+}
+
+bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a, cudaStream_t stream)
+{
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return e;
+    if (device < 0 || device >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    e = configure(fn, device);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.M * p.C), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.nt), 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.C > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    TimedRegion timed(stream);
+    return cudaLaunchKernelEx(&cfg, fn, a);
+}
+
+// Largest row count such that M * C fits a 1-D grid.
+constexpr int64_t kMaxRows = (int64_t{1} << 31) / kMaxCluster - 1;
+
+int check_matrix(const void *p, int64_t stride, int64_t M, int64_t cols, int dtype)
+{
+    if (M > 0 && !p)
+        return GBCE_ERR_NULL;
+    if (stride < cols)
+        return GBCE_ERR_SIZE;
+    if (!aligned_to(p, elem_size(dtype)))
+        return GBCE_ERR_ALIGN;
+    return GBCE_OK;
+}
+
+int check_common(int64_t M, int64_t cols, int dtype)
+{
+    if (dtype != GBCE_F32 && dtype != GBCE_BF16)
+        return GBCE_ERR_DTYPE;
+    if (M < 0 || cols < 1 || cols > INT32_MAX || M > kMaxRows)
+        return GBCE_ERR_SIZE;
+    return GBCE_OK;
+}
+
+// Do the rows of two operands start at the same address modulo 16 bytes?
+bool same_phase(const void *a, int64_t sa, const void *b, int64_t sb, size_t esize, int64_t M)
+{
+    if ((reinterpret_cast<uintptr_t>(a) - reinterpret_cast<uintptr_t>(b)) % 16 != 0)
+        return false;
+    if (M <= 1)
+        return true;
+    return ((sa - sb) * static_cast<int64_t>(esize)) % 16 == 0;
+}
+
+}  // namespace
+}  // namespace gbce
+
+using namespace gbce;
+
+extern "C" int ce_fwd_bwd(void *logits, int64_t stride, const int64_t *targets, float *loss,
+                          int64_t M, int64_t V, int64_t ignore_index, int dtype,
+                          gbce_stream_t stream_)
+{
+    int st = check_common(M, V, dtype);
+    if (st)
+        return st;
+    if (!loss || (M > 0 && !targets))
+        return GBCE_ERR_NULL;
+    if ((st = check_matrix(logits, stride, M, V, dtype)))
+        return st;
+    if (!aligned_to(targets, 8) || !aligned_to(loss, 4))
+        return GBCE_ERR_ALIGN;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return map_error(e);
+    cudaMemPool_t pool;
+    if ((e = pool_for(device, &pool)) != cudaSuccess)
+        return map_error(e);
+    // scratch: [0, 16) the non-ignored count; [256, 256 + 4M) the row losses
+    void *scratch = nullptr;
+    const size_t bytes = 256 + static_cast<size_t>(M) * sizeof(float);
+    if ((e = cudaMallocFromPoolAsync(&scratch, bytes, pool, stream)) != cudaSuccess)
+        return map_error(e);
+    int *n_ptr = static_cast<int *>(scratch);
+    float *row_loss = reinterpret_cast<float *>(static_cast<char *>(scratch) + 256);
+
+    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && M > 0) {
+        const Plan p = make_plan(V, elem_size(dtype), 1, true);
+        RowArgs a{};
+        a.in0 = logits;
+        a.s0 = stride;
+        a.out = logits;
+        a.so = stride;
+        a.M = M;
+        a.cols = V;
+        a.targets = targets;
+        a.ignore_index = ignore_index;
+        a.n_ptr = n_ptr;
+        a.row_loss = row_loss;
+        a.C = p.C;
+        a.per_vec = p.per_vec;
+        a.chunk_vec = p.chunk_vec;
+        e = launch_rows(pick<Op::CE>(dtype, p.resident, p.nt), p, a, stream);
+    }
+    if (e == cudaSuccess) {
+        ce_mean_kernel<1024><<<1, 1024, 0, stream>>>(row_loss, M, n_ptr, loss);
+        e = cudaGetLastError();
+    }
+    cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e == cudaSuccess)
+        e = ef;
+    return map_error(e);
+}
+
+extern "C" int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_stride, int64_t M,
+                           int64_t N, int dtype, gbce_stream_t stream_)
+{
+    int st = check_common(M, N, dtype);
+    if (st)
+        return st;
+    if ((st = check_matrix(x, x_stride, M, N, dtype)) || (st = check_matrix(y, y_stride, M, N, dtype)))
+        return st;
+    if (M == 0)
+        return GBCE_OK;
+    const size_t es = elem_size(dtype);
+    const Plan p = make_plan(N, es, 1, same_phase(x, x_stride, y, y_stride, es, M));
+    RowArgs a{};
+    a.in0 = x;
+    a.s0 = x_stride;
+    a.out = y;
+    a.so = y_stride;
+    a.M = M;
+    a.cols = N;
+    a.C = p.C;
+    a.per_vec = p.per_vec;
+    a.chunk_vec = p.chunk_vec;
+    return map_error(launch_rows(pick<Op::SoftmaxFwd>(dtype, p.resident, p.nt), p, a,
+                                 reinterpret_cast<cudaStream_t>(stream_)));
+}
+
+extern "C" int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int64_t dy_stride,
+                           void *dx, int64_t dx_stride, int64_t M, int64_t N, int dtype,
+                           gbce_stream_t stream_)
+{
+    int st = check_common(M, N, dtype);
+    if (st)
+        return st;
+    if ((st = check_matrix(y, y_stride, M, N, dtype)) ||
+        (st = check_matrix(dy, dy_stride, M, N, dtype)) ||
+        (st = check_matrix(dx, dx_stride, M, N, dtype)))
+        return st;
+    if (M == 0)
+        return GBCE_OK;
+    const size_t es = elem_size(dtype);
+    const bool aligned = same_phase(y, y_stride, dy, dy_stride, es, M) &&
+                         same_phase(y, y_stride, dx, dx_stride, es, M);
+    const Plan p = make_plan(N, es, 2, aligned);
+    RowArgs a{};
+    a.in0 = y;
+    a.s0 = y_stride;
+    a.in1 = dy;
+    a.s1 = dy_stride;
+    a.out = dx;
+    a.so = dx_stride;
+    a.M = M;
+    a.cols = N;
+    a.C = p.C;
+    a.per_vec = p.per_vec;
+    a.chunk_vec = p.chunk_vec;
+    return map_error(launch_rows(pick<Op::SoftmaxBwd>(dtype, p.resident, p.nt), p, a,
+                                 reinterpret_cast<cudaStream_t>(stream_)));
+}
+
+extern "C" int gbce_last_error(gbce_stream_t stream_)
+{
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_));
+    if (e != cudaSuccess)
+        return map_error(e);
+    unsigned int flags = 0;
+    const unsigned int zero = 0;
+    e = cudaMemcpyFromSymbol(&flags, g_flags, sizeof flags);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(g_flags, &zero, sizeof zero);
+    if (e != cudaSuccess)
+        return map_error(e);
+    if (flags & kFlagBadTarget)
+        return GBCE_ERR_BAD_TARGET;
+    if (flags & kFlagTimeout)
+        return GBCE_ERR_TIMEOUT;
+    return GBCE_OK;
+}
+
+extern "C" const char *gbce_status_string(int status)
+{
+    switch (status) {
+    case GBCE_OK: return "success";
+    case GBCE_ERR_NULL: return "a required pointer is NULL";
+    case GBCE_ERR_SIZE: return "invalid size: M < 0, cols < 1, stride < cols, or beyond the limits";
+    case GBCE_ERR_DTYPE: return "unknown dtype";
+    case GBCE_ERR_ALIGN: return "a pointer is not aligned to its element size";
+    case GBCE_ERR_CUDA: return "a CUDA runtime call failed";
+    case GBCE_ERR_BAD_TARGET: return "a target is outside [0, V) and is not ignore_index";
+    case GBCE_ERR_TIMEOUT: return "a bounded wait for an asynchronous copy gave up";
+    case GBCE_ERR_NO_DEVICE: return "no usable CUDA device";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int gbce_timing_enable(int on)
+{
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    g_timing_on.store(on ? 1 : 0);
+    if (!on) {
+        for (auto &pr : g_timing_pending) {
+            g_event_free.push_back(pr.first);
+            g_event_free.push_back(pr.second);
+        }
+        g_timing_pending.clear();
+    }
+    return GBCE_OK;
+}
+
+extern "C" int gbce_timing_read(double *total_ms, int64_t *launches)
+{
+    if (!total_ms || !launches)
+        return GBCE_ERR_NULL;
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    double sum = 0.0;
+    int64_t count = 0;
+    cudaError_t err = cudaSuccess;
+    for (auto &pr : g_timing_pending) {
+        cudaError_t e = cudaEventSynchronize(pr.second);
+        float ms = 0.f;
+        if (e == cudaSuccess)
+            e = cudaEventElapsedTime(&ms, pr.first, pr.second);
+        if (e != cudaSuccess && err == cudaSuccess)
+            err = e;
+        sum += ms;
+        ++count;
+        g_event_free.push_back(pr.first);
+        g_event_free.push_back(pr.second);
+    }
+    g_timing_pending.clear();
+    *total_ms = sum;
+    *launches = count;
+    return map_error(err);
+}

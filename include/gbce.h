@@ -1,0 +1,144 @@
+/*
+ * gbce: fused hard-label cross-entropy and row softmax for NVIDIA GB300 (sm_103a).
+ *
+ * Plain C ABI.  Every pointer argument of the compute calls is DEVICE memory
+ * owned by the caller; the library keeps no reference after a call returns.
+ * Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream), makes no host synchronisation, and launches only
+ * this library's own kernels.  The calling thread's current CUDA device must
+ * be the device that owns the buffers.
+ *
+ * Layout: a matrix argument is M rows of `cols` elements, row r starting at
+ * element r * stride of the pointer (row-major, unit column stride, stride in
+ * ELEMENTS, stride >= cols).  Columns at and beyond `cols` are never read or
+ * written.  Row offsets are computed in 64-bit arithmetic.
+ *
+ * Return value: GBCE_OK (0) or a gbce_status code.  Argument errors are
+ * detected on the host before anything is launched and leave every buffer
+ * untouched.  Errors that only the device can see (an out-of-range target, a
+ * bounded wait that gave up) are raised as sticky per-device flags that
+ * gbce_last_error() reports.
+ */
+#ifndef GBCE_H
+#define GBCE_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GBCE_API __attribute__((visibility("default")))
+#else
+#define GBCE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st *gbce_stream_t;
+
+/* Element types of the logits / softmax operands. */
+enum gbce_dtype {
+    GBCE_F32 = 0,  /* IEEE binary32 */
+    GBCE_BF16 = 1  /* bfloat16; arithmetic is fp32, results are rounded to nearest even */
+};
+
+enum gbce_status {
+    GBCE_OK = 0,
+    GBCE_ERR_NULL = 1,        /* a required pointer is NULL */
+    GBCE_ERR_SIZE = 2,        /* M < 0, cols < 1, stride < cols, or a size beyond the limits */
+    GBCE_ERR_DTYPE = 3,       /* dtype is not a gbce_dtype */
+    GBCE_ERR_ALIGN = 4,       /* a pointer is not aligned to its element size */
+    GBCE_ERR_CUDA = 5,        /* a CUDA runtime call (allocation, launch) failed */
+    GBCE_ERR_BAD_TARGET = 6,  /* device flag: a target outside [0, V) that is not ignore_index */
+    GBCE_ERR_TIMEOUT = 7,     /* device flag: a bounded wait on an asynchronous copy gave up */
+    GBCE_ERR_NO_DEVICE = 8    /* no usable CUDA device */
+};
+
+/*
+ * ce_fwd_bwd -- fused hard-label cross-entropy, forward and backward in one call.
+ *
+ * Defined by: Liger-Kernel, src/liger_kernel/ops/cross_entropy.py,
+ * liger_cross_entropy_kernel (steps 1-6) and LigerCrossEntropyFunction.forward:
+ * hard labels, mean reduction over the non-ignored rows, PyTorch
+ * CrossEntropyLoss semantics, gradient stored in place over the input.
+ *
+ *   logits        [M, stride] of dtype, rows of V logits.  READ, then OVERWRITTEN
+ *                 IN PLACE with dL/dlogits:
+ *                   g[r,i] = (softmax(x_r)_i - [i == t_r]) / n     (t_r != ignore_index)
+ *                   g[r,i] = 0                                      (t_r == ignore_index)
+ *                 n = number of rows whose target is not ignore_index, over the
+ *                 whole call.  Elements outside [0, V) of each row are untouched.
+ *   stride        row stride of logits in elements (>= V).
+ *   targets       [M] int64 class indices (PyTorch convention), read only.
+ *   loss          one float: receives L = sum_r l_r / n with
+ *                 l_r = max(x_r) + ln sum_i exp(x_r,i - max(x_r)) - x_r,t_r.
+ *                 When n == 0 (M == 0 or every row ignored) L is NaN (0/0).
+ *   M, V          rows and classes; M >= 0, 1 <= V < 2^31, M * V may exceed 2^32.
+ *   ignore_index  target value that marks a row as ignored (PyTorch uses -100).
+ *   dtype         GBCE_F32 or GBCE_BF16 (logits; targets are always int64).
+ *
+ * A target that is neither ignore_index nor in [0, V) leaves its row
+ * unmodified, makes L NaN and raises GBCE_ERR_BAD_TARGET in gbce_last_error().
+ * Temporary device memory (M floats and a counter) is taken stream-ordered
+ * from a library-owned memory pool and returned within the call's stream work.
+ * Results are deterministic: the same inputs give the same bits.
+ */
+GBCE_API int ce_fwd_bwd(void *logits, int64_t stride, const int64_t *targets, float *loss, int64_t M,
+               int64_t V, int64_t ignore_index, int dtype, gbce_stream_t stream);
+
+/*
+ * softmax_fwd -- row-wise safe softmax, y = exp(x - max x) / sum exp(x - max x).
+ *
+ * Defined by: "python sum function examples (triton.language)", _softmax and
+ * softmax_kernel (one program per row, separate input and output row strides).
+ *
+ *   x [M, x_stride] read; y [M, y_stride] written (cols 0..N-1 of each row).
+ *   y may be the same buffer as x (same stride): each row is read completely
+ *   before any of it is written.  Other partial overlaps are not allowed.
+ */
+GBCE_API int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_stride, int64_t M, int64_t N,
+                int dtype, gbce_stream_t stream);
+
+/*
+ * softmax_bwd -- softmax backward, dx = y * (dy - sum(y * dy)) per row.
+ *
+ * Defined by: "python sum function examples (triton.language)", _backward
+ * (fused softmax backward), dense rows and scale 1.
+ *
+ *   y  [M, y_stride]  softmax output, read.
+ *   dy [M, dy_stride] upstream gradient, read.
+ *   dx [M, dx_stride] written.  dx may be the same buffer as dy (same stride),
+ *   as in the page's in-place store; other overlaps are not allowed.
+ */
+GBCE_API int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int64_t dy_stride, void *dx,
+                int64_t dx_stride, int64_t M, int64_t N, int dtype, gbce_stream_t stream);
+
+/*
+ * gbce_last_error -- synchronise `stream`, then read and clear the current
+ * device's sticky error flags.  Returns GBCE_OK, GBCE_ERR_BAD_TARGET,
+ * GBCE_ERR_TIMEOUT (when both are set, BAD_TARGET), or GBCE_ERR_CUDA when the
+ * synchronisation itself failed.
+ */
+GBCE_API int gbce_last_error(gbce_stream_t stream);
+
+/* gbce_status_string -- a static, NUL-terminated description of a status code. */
+GBCE_API const char *gbce_status_string(int status);
+
+/*
+ * Kernel timing for benchmarks.  While enabled, every ce_fwd_bwd /
+ * softmax_fwd / softmax_bwd call brackets its row kernel (the kernel that
+ * streams the logits) with two CUDA events on the call's stream.
+ * gbce_timing_read() waits for those events, returns the summed kernel time in
+ * milliseconds and the number of bracketed launches, and forgets them.
+ * gbce_timing_enable(0) drops unread records.  Not thread safe with
+ * concurrent calls from several host threads.
+ */
+GBCE_API int gbce_timing_enable(int on);
+GBCE_API int gbce_timing_read(double *total_ms, int64_t *launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBCE_H */

@@ -1,0 +1,108 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every
+entry point declared in include/gbce.h, and rejects bad arguments on the host
+(before any CUDA call, so this runs on a machine without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from cross_entropy_loss_ce_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbce.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*GBCE_API\s+(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\([^;]*\)\s*;", text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = gbuild.build()
+    lib = ctypes.CDLL(path)
+    i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.ce_fwd_bwd.argtypes = [p, i64, p, p, i64, i64, i64, ci, p]
+    lib.softmax_fwd.argtypes = [p, i64, p, i64, i64, i64, ci, p]
+    lib.softmax_bwd.argtypes = [p, i64, p, i64, p, i64, i64, i64, ci, p]
+    lib.gbce_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    assert {"ce_fwd_bwd", "softmax_fwd", "softmax_bwd", "gbce_last_error",
+            "gbce_status_string", "gbce_timing_enable", "gbce_timing_read"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in gbce.h but not exported"
+
+
+def test_only_the_abi_is_exported(lib):
+    # hidden visibility: nothing but the declared C names (and runtime-internal
+    # symbols, if any) should be visible; spot-check a kernel name is not.
+    assert not hasattr(lib, "_ZN4gbce14ce_mean_kernelILi1024EEEvPKflPKiPf")
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = lib.gbce_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.gbce_status_string(99).decode() == "unknown status"
+
+
+FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
+
+
+@pytest.mark.parametrize("args,code", [
+    # (logits, stride, targets, loss, M, V, ignore_index, dtype) -> status
+    ((None, 10, FAKE, FAKE, 4, 10, -100, 0), 1),        # NULL logits
+    ((FAKE, 10, None, FAKE, 4, 10, -100, 0), 1),        # NULL targets
+    ((FAKE, 10, FAKE, None, 4, 10, -100, 0), 1),        # NULL loss
+    ((FAKE, 10, FAKE, FAKE, 4, 0, -100, 0), 2),         # V < 1
+    ((FAKE, 9, FAKE, FAKE, 4, 10, -100, 0), 2),         # stride < V
+    ((FAKE, 10, FAKE, FAKE, -1, 10, -100, 0), 2),       # M < 0
+    ((FAKE, 10, FAKE, FAKE, 4, 2**31, -100, 0), 2),     # V beyond int32
+    ((FAKE, 10, FAKE, FAKE, 4, 10, -100, 2), 3),        # unknown dtype
+    ((FAKE + 2, 10, FAKE, FAKE, 4, 10, -100, 0), 4),    # fp32 logits not 4-byte aligned
+    ((FAKE + 1, 10, FAKE, FAKE, 4, 10, -100, 1), 4),    # bf16 logits not 2-byte aligned
+    ((FAKE, 10, FAKE + 4, FAKE, 4, 10, -100, 0), 4),    # targets not 8-byte aligned
+])
+def test_ce_rejects_bad_arguments(lib, args, code):
+    assert lib.ce_fwd_bwd(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 8, FAKE, 8, 2, 8, 0), 1),
+    ((FAKE, 8, None, 8, 2, 8, 0), 1),
+    ((FAKE, 7, FAKE, 8, 2, 8, 0), 2),
+    ((FAKE, 8, FAKE, 7, 2, 8, 0), 2),
+    ((FAKE, 8, FAKE, 8, 2, 0, 0), 2),
+    ((FAKE, 8, FAKE, 8, 2, 8, 5), 3),
+    ((FAKE + 2, 8, FAKE, 8, 2, 8, 0), 4),
+])
+def test_softmax_fwd_rejects_bad_arguments(lib, args, code):
+    assert lib.softmax_fwd(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 8, FAKE, 8, FAKE, 8, 2, 8, 0), 1),
+    ((FAKE, 8, None, 8, FAKE, 8, 2, 8, 0), 1),
+    ((FAKE, 8, FAKE, 8, None, 8, 2, 8, 0), 1),
+    ((FAKE, 8, FAKE, 6, FAKE, 8, 2, 8, 0), 2),
+    ((FAKE, 8, FAKE, 8, FAKE, 8, -3, 8, 0), 2),
+    ((FAKE, 8, FAKE, 8, FAKE, 8, 2, 8, -1), 3),
+    ((FAKE, 8, FAKE, 8, FAKE + 1, 8, 2, 8, 1), 4),
+])
+def test_softmax_bwd_rejects_bad_arguments(lib, args, code):
+    assert lib.softmax_bwd(*args, None) == code
+
+
+def test_empty_softmax_is_a_noop(lib):
+    # M == 0 returns success without touching the device
+    assert lib.softmax_fwd(None, 8, None, 8, 0, 8, 0, None) == 0
+    assert lib.softmax_bwd(None, 8, None, 8, None, 8, 0, 8, 1, None) == 0

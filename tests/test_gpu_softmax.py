@@ -1,0 +1,83 @@
+"""CUDA row softmax forward and backward against the double-precision oracle (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import cross_entropy_loss_ce_gb300 as gbce
+import oracle
+import workloads
+from gpu_util import host, require_gpu
+from parity import check_softmax, check_softmax_bwd
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("N", workloads.SOFTMAX_NS)
+def test_softmax_reduced_rows(dtype, N):
+    require_gpu()
+    x, y, dy = workloads.make_softmax_inputs(64, N, dtype)
+    ref_y = oracle.softmax_fwd(host(x))
+    ref_dx = oracle.softmax_bwd(host(y), host(dy))
+    got_y = gbce.softmax_fwd(x.cuda())
+    got_dx = gbce.softmax_bwd(y.cuda(), dy.cuda())
+    assert gbce.last_error() == gbce.OK
+    check_softmax(got_y, ref_y, dtype, f"softmax N={N}")
+    check_softmax_bwd(got_dx, ref_dx, y, dy, dtype, f"softmax bwd N={N}")
+
+
+@pytest.mark.parametrize("N", workloads.SOFTMAX_NS)
+def test_softmax_full_size_sampled_rows(N):
+    """All 4096 rows on the GPU; rows sampled for the oracle."""
+    require_gpu()
+    x, y, dy = workloads.make_softmax_inputs(workloads.SOFTMAX_M, N, device="cuda")
+    rows = np.unique(np.concatenate([[0, workloads.SOFTMAX_M - 1],
+                                     np.random.default_rng(N).choice(workloads.SOFTMAX_M, 30)]))
+    ref_y = oracle.softmax_fwd(host(x), rows=rows)
+    ref_dx = oracle.softmax_bwd(host(y), host(dy), rows=rows)
+    got_y = gbce.softmax_fwd(x)
+    got_dx = gbce.softmax_bwd(y, dy)
+    assert gbce.last_error() == gbce.OK
+    r = torch.as_tensor(rows, device="cuda")
+    check_softmax(got_y[r], ref_y, torch.float32)
+    check_softmax_bwd(got_dx[r], ref_dx, y[r], dy[r], torch.float32)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("N", [1, 3, 7, 8, 9, 33, 1000, 65537, 300001, 1000003])
+def test_softmax_shapes_strides_and_aliasing(dtype, N):
+    """Ragged N, the in-place forms (y = x, dx = dy), and operands whose rows
+    sit at different 16-byte phases (the streaming fallback)."""
+    require_gpu()
+    M = 5 if N < 500000 else 2
+    g = torch.Generator().manual_seed(N)
+    x = torch.randn((M, N), generator=g).to(dtype)
+    e = torch.rand((M, N), generator=g) + 0.01
+    y = (e / e.sum(1, keepdim=True)).to(dtype)
+    dy = torch.randn((M, N), generator=g).to(dtype)
+    ref_y = oracle.softmax_fwd(host(x))
+    ref_dx = oracle.softmax_bwd(host(y), host(dy))
+    # in place
+    xd = x.cuda()
+    gbce.softmax_fwd(xd, xd)
+    check_softmax(xd, ref_y, dtype, f"in-place softmax N={N}")
+    dyd = dy.cuda()
+    gbce.softmax_bwd(y.cuda(), dyd, dyd)
+    check_softmax_bwd(dyd, ref_dx, y, dy, dtype, f"in-place softmax bwd N={N}")
+    # x padded by one element per row, y contiguous: different phases
+    xp = torch.zeros((M, N + 1), dtype=dtype, device="cuda")
+    xp[:, 1:] = x.cuda()
+    yo = gbce.softmax_fwd(xp[:, 1:])
+    check_softmax(yo, ref_y, dtype, f"shifted softmax N={N}")
+    dyp = torch.zeros((M, N + 3), dtype=dtype, device="cuda")
+    dyp[:, 3:] = dy.cuda()
+    dxo = gbce.softmax_bwd(y.cuda(), dyp[:, 3:])
+    check_softmax_bwd(dxo, ref_dx, y, dy, dtype, f"shifted softmax bwd N={N}")
+    assert gbce.last_error() == gbce.OK
+
+
+def test_softmax_empty():
+    require_gpu()
+    x = torch.empty((0, 16), device="cuda")
+    assert gbce.softmax_fwd(x).shape == (0, 16)
+    assert gbce.softmax_bwd(x, x).shape == (0, 16)
