@@ -404,7 +404,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gbce", "reference"], default="gbce")
     ap.add_argument("--workload", choices=list(workloads.CE_WORKLOADS), default=DEFAULT_WORKLOAD)
-    ap.add_argument("--cpu-rows", type=int, default=4096)
+    ap.add_argument("--cpu-rows", type=int, default=16384)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-softmax", action="store_true")
