@@ -220,7 +220,7 @@ def run_reference(args, ws, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "V": w.V, "logits_dtype": str(w.dtype),
+        "config": {"workload": w.name + (f" (first {w.M} rows)" if args.rows else ""), "M": w.M, "V": w.V, "logits_dtype": str(w.dtype),
                    "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
                          "sample": f"{sample} rows of {w.name} per step (seeded CPU draw), "
@@ -328,6 +328,8 @@ def run_gbce(args, ws, rank, local):
     gbce.load_library()
     torch.cuda.set_device(local)
     w = workloads.CE_WORKLOADS[args.workload]
+    if args.rows:
+        w = w.with_rows(args.rows)
     xd0, td = workloads.make_ce_inputs(w, "cuda")
     t_host = td.cpu().numpy()
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -354,7 +356,7 @@ def run_gbce(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "V": w.V, "ignore_frac": w.ignore_frac,
+        "config": {"workload": w.name + (f" (first {w.M} rows)" if args.rows else ""), "M": w.M, "V": w.V, "ignore_frac": w.ignore_frac,
                    "logits": f"N(0,{w.std}^2)" + (f" + {w.spike} spike/row" if w.spike else ""),
                    "l2": "inputs (4.2 GB) larger than L2, and a 512 MB L2 flush before each step",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
@@ -404,6 +406,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gbce", "reference"], default="gbce")
     ap.add_argument("--workload", choices=list(workloads.CE_WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--rows", type=int, default=0,
+                    help="run the first ROWS rows of the workload only (profiling a small case)")
     ap.add_argument("--cpu-rows", type=int, default=16384)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
