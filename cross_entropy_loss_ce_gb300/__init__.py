@@ -148,3 +148,32 @@ def timing_read():
     ms, n = ctypes.c_double(), ctypes.c_int64()
     _check(load_library().gbce_timing_read(ctypes.byref(ms), ctypes.byref(n)), "gbce_timing_read")
     return ms.value, n.value
+
+
+def ce_fwd_bwd_noalloc(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+                       loss: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """ce_fwd_bwd for callers that cannot let the library allocate device memory.
+
+    Same results; the temporary storage is a fixed static device array inside
+    the library (M <= 65536 rows), shared by every call on the device, so
+    calls that overlap on the GPU must be serialised by the caller.  ``loss``
+    is allocated here by torch when not given.
+    """
+    lib = load_library()
+    fn = lib.ce_fwd_bwd_noalloc
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    lp, stride, M, V = _matrix(logits, "logits")
+    if targets.dtype != torch.int64 or targets.dim() != 1 or targets.shape[0] != M:
+        raise ValueError("targets must be int64 of shape [M]")
+    if M and (not targets.is_cuda or not targets.is_contiguous()):
+        raise ValueError("targets must be a contiguous CUDA tensor")
+    if loss is None:
+        loss = torch.empty((), dtype=torch.float32, device=logits.device)
+    elif loss.dtype != torch.float32 or loss.numel() != 1 or not loss.is_cuda:
+        raise ValueError("loss must be a one-element float32 CUDA tensor")
+    rc = fn(lp, stride, targets.data_ptr(), loss.data_ptr(), M, V, int(ignore_index),
+            DTYPES[logits.dtype], _stream_handle(stream))
+    _check(rc, "ce_fwd_bwd_noalloc")
+    return loss

@@ -473,3 +473,98 @@ extern "C" int gbce_timing_read(double *total_ms, int64_t *launches)
     *launches = count;
     return map_error(err);
 }
+
+// ---------------------------------------------------------------------------
+// ce_fwd_bwd_noalloc: the same three launches as ce_fwd_bwd, with their
+// temporary storage in a fixed static device array instead of the pool.
+
+namespace gbce {
+namespace {
+
+constexpr int64_t kNoAllocMaxRows = GBCE_NOALLOC_MAX_ROWS;
+constexpr size_t kNoAllocHeader = 256;  // [0, 4): the non-ignored count
+
+// [0, 256): header; [256, 256 + 4 * kNoAllocMaxRows): the row losses.
+static __device__ __align__(256) unsigned char
+    g_noalloc_scratch[kNoAllocHeader + kNoAllocMaxRows * sizeof(float)];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on `device` (the current device),
+// looked up once per device.  The symbol's name in host code is only a
+// host-side handle and must never be handed to a kernel.
+cudaError_t noalloc_scratch(int device, void **out)
+{
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[device]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return e;
+        g_noalloc_addr[device] = p;
+    }
+    *out = g_noalloc_addr[device];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace gbce
+
+extern "C" int ce_fwd_bwd_noalloc(void *logits, int64_t stride, const int64_t *targets,
+                                  float *loss, int64_t M, int64_t V, int64_t ignore_index,
+                                  int dtype, gbce_stream_t stream_)
+{
+    int st = check_common(M, V, dtype);
+    if (st)
+        return st;
+    if (!loss || (M > 0 && !targets))
+        return GBCE_ERR_NULL;
+    if ((st = check_matrix(logits, stride, M, V, dtype)))
+        return st;
+    if (!aligned_to(targets, 8) || !aligned_to(loss, 4))
+        return GBCE_ERR_ALIGN;
+    if (M > kNoAllocMaxRows)
+        return GBCE_ERR_SIZE;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return map_error(e);
+    if (device < 0 || device >= kMaxDevices)
+        return GBCE_ERR_CUDA;
+    void *scratch = nullptr;
+    if ((e = noalloc_scratch(device, &scratch)) != cudaSuccess)
+        return map_error(e);
+    // ce_count_kernel overwrites the count and the row kernel writes the loss
+    // of every row 0..M-1 before ce_mean_kernel reads it: nothing needs clearing.
+    int *n_ptr = static_cast<int *>(scratch);
+    float *row_loss = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocHeader);
+
+    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && M > 0) {
+        const Plan p = make_plan(V, elem_size(dtype), 1, true);
+        RowArgs a{};
+        a.in0 = logits;
+        a.s0 = stride;
+        a.out = logits;
+        a.so = stride;
+        a.M = M;
+        a.cols = V;
+        a.targets = targets;
+        a.ignore_index = ignore_index;
+        a.n_ptr = n_ptr;
+        a.row_loss = row_loss;
+        a.C = p.C;
+        a.per_vec = p.per_vec;
+        a.chunk_vec = p.chunk_vec;
+        e = launch_rows(pick<Op::CE>(dtype, p.resident, p.nt), p, a, stream);
+    }
+    if (e == cudaSuccess) {
+        ce_mean_kernel<1024><<<1, 1024, 0, stream>>>(row_loss, M, n_ptr, loss);
+        e = cudaGetLastError();
+    }
+    return map_error(e);
+}

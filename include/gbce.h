@@ -87,6 +87,37 @@ enum gbce_status {
 GBCE_API int ce_fwd_bwd(void *logits, int64_t stride, const int64_t *targets, float *loss, int64_t M,
                int64_t V, int64_t ignore_index, int dtype, gbce_stream_t stream);
 
+/* Largest row count M that ce_fwd_bwd_noalloc accepts. */
+#define GBCE_NOALLOC_MAX_ROWS 65536
+
+/*
+ * ce_fwd_bwd_noalloc -- ce_fwd_bwd that allocates no device memory.
+ *
+ * The pages have no counterpart of this entry point.  It is for callers that
+ * cannot have a library allocate device memory at call time: processes whose
+ * caching allocator has reserved the device's memory up front, serving
+ * runtimes that forbid allocation after start-up to keep a fixed memory
+ * budget, and devices or drivers without stream-ordered memory pools
+ * (cudaDevAttrMemoryPoolsSupported == 0).
+ *
+ * Arguments, results, layout and errors are those of ce_fwd_bwd, computed by
+ * the same kernels.  The temporary storage (the non-ignored count and M row
+ * losses) lives instead in one fixed array of static device memory inside
+ * this library, about 256 KB, which every GPU that loads the library holds
+ * until the process exits.  Hence:
+ *   - M > GBCE_NOALLOC_MAX_ROWS is rejected with GBCE_ERR_SIZE before any launch;
+ *   - no cudaMalloc, cudaMallocAsync, cudaFree or other allocating call is made;
+ *   - every call on a device shares that array and leaves its contents behind;
+ *     each call overwrites every entry it reads, so no state carries over, but
+ *     calls whose work overlaps on the GPU (on different streams, or from
+ *     different host threads) race on it and must be serialised by the caller;
+ *   - the first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ */
+GBCE_API int ce_fwd_bwd_noalloc(void *logits, int64_t stride, const int64_t *targets, float *loss,
+                                int64_t M, int64_t V, int64_t ignore_index, int dtype,
+                                gbce_stream_t stream);
+
 /*
  * softmax_fwd -- row-wise safe softmax, y = exp(x - max x) / sum exp(x - max x).
  *
