@@ -120,6 +120,26 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
     return r;
 }
 
+// Store 16 bytes into shared memory of a peer CTA (a shared::cluster address)
+// and count them on that CTA's mbarrier (also a shared::cluster address).
+__device__ __forceinline__ void st_async_f4(uint32_t remote, float4 v, uint32_t remote_bar)
+{
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(remote),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_any()
+{
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_any()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr)
 {
     float2 v;

@@ -18,64 +18,96 @@ namespace gbce {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int64_t kSliceTarget = 64 * 1024;   // staged bytes per CTA: three CTAs per SM
-constexpr int64_t kSliceMax = 200 * 1024;     // largest slice staged in shared memory
+constexpr int64_t kResidentMax = 64 * 1024;   // rows up to this many staged bytes: resident kernel
+constexpr int64_t kSliceMax = 200 * 1024;     // dynamic shared memory limit set on every kernel
 constexpr int kMaxCluster = 16;
+constexpr int64_t kStreamSlice = 64 * 1024;   // bytes of a row per CTA in the streaming fallback
+constexpr int64_t kRingBytes = 192 * 1024;    // ring capacity per CTA (one CTA per SM)
+constexpr int kRingWarps = 16;                // consumer warps of the ring kernel
+constexpr int kRingVpt1 = 4;                  // vectors per consumer thread and slot, one operand
+constexpr int kRingVpt2 = 2;                  // the same, two operands (softmax backward)
+constexpr int64_t kL2Budget = 48ll << 20;     // bytes of rows between their two reads, all SMs
 
 size_t elem_size(int dtype) { return dtype == GBCE_F32 ? 4 : 2; }
 
+std::mutex g_sm_mu;
+int g_sm_count[kMaxDevices] = {};
+
+// Multiprocessors of the current device (cached per device; 0 if unknown).
+int64_t current_sm_count()
+{
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+        return 0;
+    std::lock_guard<std::mutex> lk(g_sm_mu);
+    if (!g_sm_count[device]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+            return 0;
+        g_sm_count[device] = n;
+    }
+    return g_sm_count[device];
+}
+
 // ---------------------------------------------------------------------------
-// launch plan
+// launch plan: the kernel regime is chosen by the row length
+
+enum class Kind { Resident, Ring, Streaming };
 
 struct Plan {
-    bool resident;  // slices staged in shared memory (else the streaming fallback)
+    Kind kind;
     int C;          // CTAs per row = cluster size
     int nt;         // threads per CTA
-    int per_vec;    // 16-byte vectors per slice
-    int chunk_vec;  // vectors per bulk copy
+    int per_vec;    // resident: 16-byte vectors staged per operand
+    int chunk_vec;  // resident: vectors per bulk copy; ring: vectors per slot
+    int nslot;      // ring: slots
     size_t smem;    // dynamic shared memory per CTA
 };
 
-int threads_for(int64_t per_vec)
-{
-    return per_vec >= 2048 ? 512 : (per_vec >= 512 ? 256 : 128);
-}
-
-// cols elements of esize bytes per operand, nbuf operands staged per row;
-// `aligned`: all operands of every row share their address modulo 16 bytes.
+// cols elements of esize bytes per operand, nbuf operands per row; `aligned`:
+// all operands of every row share their address modulo 16 bytes.
 Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned)
 {
     Plan p{};
-    const int64_t nvec = cols * static_cast<int64_t>(esize) / 16;  // >= whole vectors of any row
-    int C = 1;
-    int64_t per = nvec;
-    while (C < kMaxCluster && per * 16 * nbuf > kSliceTarget) {
-        C *= 2;
-        per = (nvec + C - 1) / C;
-    }
-    if (per < 1)
-        per = 1;
-    p.C = C;
-    p.resident = aligned && per * 16 * nbuf <= kSliceMax;
-    if (!p.resident) {
-        // streaming fallback: enough CTAs that each streams ~64 KB of a row
-        int64_t bytes = cols * static_cast<int64_t>(esize);
-        int Cs = 1;
-        while (Cs < kMaxCluster && bytes / Cs > kSliceTarget)
-            Cs *= 2;
-        p.C = Cs;
+    const int64_t row_bytes = cols * static_cast<int64_t>(esize);
+    if (!aligned) {
+        // streaming fallback: a cluster per row, each CTA streaming ~64 KB of it
+        p.kind = Kind::Streaming;
+        p.C = 1;
+        while (p.C < kMaxCluster && row_bytes / p.C > kStreamSlice)
+            p.C *= 2;
         p.nt = 512;
-        p.per_vec = 0;
-        p.chunk_vec = 0;
-        p.smem = 0;
         return p;
     }
-    p.per_vec = static_cast<int>(per);
-    p.nt = threads_for(per);
-    int64_t chunk = (per + kMaxChunks - 1) / kMaxChunks;
-    chunk = (chunk + p.nt - 1) / p.nt * p.nt;
-    p.chunk_vec = static_cast<int>(chunk);
-    p.smem = static_cast<size_t>(per) * 16 * nbuf;
+    const int64_t nvec = row_bytes / 16;  // >= whole vectors of any row
+    if (nvec * 16 * nbuf <= kResidentMax) {
+        // short rows: one CTA per row holds the row, three CTAs per SM
+        p.kind = Kind::Resident;
+        p.C = 1;
+        p.per_vec = static_cast<int>(nvec > 0 ? nvec : 1);
+        p.nt = p.per_vec >= 512 ? 256 : 128;
+        int64_t chunk = (p.per_vec + kMaxChunks - 1) / kMaxChunks;
+        chunk = (chunk + p.nt - 1) / p.nt * p.nt;
+        p.chunk_vec = static_cast<int>(chunk);
+        p.smem = static_cast<size_t>(p.per_vec) * 16 * nbuf;
+        return p;
+    }
+    // long rows: each SM streams one row slice at a time through the ring and
+    // reads it twice; split rows across a cluster until the slices between
+    // their two reads fit in L2
+    p.kind = Kind::Ring;
+    const int64_t sms = current_sm_count();
+    p.C = 1;
+    while (p.C < kMaxCluster && sms * row_bytes * nbuf / p.C > kL2Budget)
+        p.C *= 2;
+    p.nt = (kRingWarps + 1) * 32;
+    const int vpt = nbuf == 2 ? kRingVpt2 : kRingVpt1;
+    const int64_t chunk_bytes = static_cast<int64_t>(kRingWarps) * 32 * vpt * 16;
+    p.chunk_vec = static_cast<int>(chunk_bytes / 16);
+    p.nslot = static_cast<int>(kRingBytes / (chunk_bytes * nbuf));
+    if (p.nslot > kRingMaxSlots)
+        p.nslot = kRingMaxSlots;
+    p.smem = static_cast<size_t>(p.nslot) * chunk_bytes * nbuf;
     return p;
 }
 
@@ -85,23 +117,22 @@ Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned)
 using KernelFn = void (*)(const RowArgs);
 
 template <Op OP, typename T>
-KernelFn pick_kernel(bool resident, int nt)
+KernelFn pick_kernel(const Plan &p)
 {
-    if (resident) {
-        switch (nt) {
-        case 128: return rows_resident_kernel<OP, T, 128>;
-        case 256: return rows_resident_kernel<OP, T, 256>;
-        default: return rows_resident_kernel<OP, T, 512>;
-        }
+    switch (p.kind) {
+    case Kind::Resident:
+        return p.nt == 128 ? rows_resident_kernel<OP, T, 128> : rows_resident_kernel<OP, T, 256>;
+    case Kind::Ring:
+        return rows_ring_kernel<OP, T, kRingWarps, OP == Op::SoftmaxBwd ? kRingVpt2 : kRingVpt1>;
+    default:
+        return rows_streaming_kernel<OP, T, 512>;
     }
-    return rows_streaming_kernel<OP, T, 512>;
 }
 
 template <Op OP>
-KernelFn pick(int dtype, bool resident, int nt)
+KernelFn pick(int dtype, const Plan &p)
 {
-    return dtype == GBCE_F32 ? pick_kernel<OP, float>(resident, nt)
-                             : pick_kernel<OP, __nv_bfloat16>(resident, nt);
+    return dtype == GBCE_F32 ? pick_kernel<OP, float>(p) : pick_kernel<OP, __nv_bfloat16>(p);
 }
 
 // Per-device one-time function attributes (large dynamic shared memory,
@@ -110,6 +141,13 @@ struct FnConfig {
     KernelFn fn;
     int device;
 };
+struct GridCache {
+    KernelFn fn;
+    int device, C, nt;
+    size_t smem;
+    int64_t clusters;  // clusters (or CTAs when C == 1) resident at once
+};
+std::vector<GridCache> g_grid;
 std::mutex g_cfg_mu;
 std::vector<FnConfig> g_cfg;
 
@@ -213,6 +251,49 @@ int map_error(cudaError_t e)
 
 bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// How many clusters of the persistent kernel fit on the device at once.
+cudaError_t resident_clusters(KernelFn fn, const Plan &p, int device, int64_t *out)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_cfg_mu);
+        for (const GridCache &c : g_grid)
+            if (c.fn == fn && c.device == device && c.C == p.C && c.nt == p.nt && c.smem == p.smem) {
+                *out = c.clusters;
+                return cudaSuccess;
+            }
+    }
+    int n = 0;
+    cudaError_t e;
+    if (p.C == 1) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, p.nt, p.smem);
+        n *= sms;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(p.C), 1, 1);
+        cfg.blockDim = dim3(static_cast<unsigned>(p.nt), 1, 1);
+        cfg.dynamicSmemBytes = p.smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    }
+    if (e != cudaSuccess)
+        return e;
+    if (n < 1)
+        return cudaErrorInvalidConfiguration;
+    std::lock_guard<std::mutex> lk(g_cfg_mu);
+    g_grid.push_back({fn, device, p.C, p.nt, p.smem, n});
+    *out = n;
+    return cudaSuccess;
+}
+
 cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a, cudaStream_t stream)
 {
     int device = 0;
@@ -224,8 +305,15 @@ cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a, cudaStream
     e = configure(fn, device);
     if (e != cudaSuccess)
         return e;
+    int64_t clusters = a.M;  // resident and streaming kernels: one CTA / cluster per row
+    if (p.kind == Kind::Ring) {
+        int64_t fit = 0;
+        if ((e = resident_clusters(fn, p, device, &fit)) != cudaSuccess)
+            return e;
+        clusters = fit < a.M ? fit : a.M;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.M * p.C), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * p.C), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(p.nt), 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
@@ -328,7 +416,8 @@ extern "C" int ce_fwd_bwd(void *logits, int64_t stride, const int64_t *targets, 
         a.C = p.C;
         a.per_vec = p.per_vec;
         a.chunk_vec = p.chunk_vec;
-        e = launch_rows(pick<Op::CE>(dtype, p.resident, p.nt), p, a, stream);
+        a.nslot = p.nslot;
+        e = launch_rows(pick<Op::CE>(dtype, p), p, a, stream);
     }
     if (e == cudaSuccess) {
         ce_mean_kernel<1024><<<1, 1024, 0, stream>>>(row_loss, M, n_ptr, loss);
@@ -362,7 +451,8 @@ extern "C" int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_s
     a.C = p.C;
     a.per_vec = p.per_vec;
     a.chunk_vec = p.chunk_vec;
-    return map_error(launch_rows(pick<Op::SoftmaxFwd>(dtype, p.resident, p.nt), p, a,
+    a.nslot = p.nslot;
+    return map_error(launch_rows(pick<Op::SoftmaxFwd>(dtype, p), p, a,
                                  reinterpret_cast<cudaStream_t>(stream_)));
 }
 
@@ -395,7 +485,8 @@ extern "C" int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int6
     a.C = p.C;
     a.per_vec = p.per_vec;
     a.chunk_vec = p.chunk_vec;
-    return map_error(launch_rows(pick<Op::SoftmaxBwd>(dtype, p.resident, p.nt), p, a,
+    a.nslot = p.nslot;
+    return map_error(launch_rows(pick<Op::SoftmaxBwd>(dtype, p), p, a,
                                  reinterpret_cast<cudaStream_t>(stream_)));
 }
 
@@ -560,7 +651,8 @@ extern "C" int ce_fwd_bwd_noalloc(void *logits, int64_t stride, const int64_t *t
         a.C = p.C;
         a.per_vec = p.per_vec;
         a.chunk_vec = p.chunk_vec;
-        e = launch_rows(pick<Op::CE>(dtype, p.resident, p.nt), p, a, stream);
+        a.nslot = p.nslot;
+        e = launch_rows(pick<Op::CE>(dtype, p), p, a, stream);
     }
     if (e == cudaSuccess) {
         ce_mean_kernel<1024><<<1, 1024, 0, stream>>>(row_loss, M, n_ptr, loss);

@@ -1,7 +1,9 @@
 // Row kernels: fused cross-entropy forward+backward, softmax forward, softmax
-// backward.  One thread-block cluster of C CTAs handles one row; each CTA
-// stages its contiguous slice of the row in shared memory with 1-D bulk (TMA)
-// copies, so the row is read from HBM once and written once.
+// backward.  Rows are staged in shared memory with 1-D bulk (TMA) copies so
+// that HBM sees one read and one write per element: short rows stay resident
+// in one CTA (rows_resident_kernel); longer rows stream twice through a
+// warp-specialised ring whose second read is served by L2, split across a
+// thread-block cluster when needed (rows_ring_kernel).
 //
 // Per row (cross-entropy; the softmax forward is the same without the target):
 //   1. target load and ignore test (Liger-Kernel cross_entropy.py,
@@ -43,6 +45,7 @@ struct RowArgs {
     int C;          // CTAs per row (cluster size)
     int per_vec;    // 16-byte vectors per CTA slice (capacity of one staged buffer)
     int chunk_vec;  // vectors per bulk copy, a multiple of the CTA's thread count
+    int nslot;      // ring slots (ring kernel)
 };
 
 // Sticky error flags of this device (kFlag* bits); defined once per library.
@@ -74,6 +77,11 @@ struct Partial {
     }
 };
 
+// ---------------------------------------------------------------------------
+// Resident form, for rows whose operands fit one CTA's shared memory (<= 64 KB
+// per row in all): one CTA per row, three CTAs per SM.  The CTA stages its row
+// with up to kMaxChunks bulk copies (one mbarrier each), runs pass 1 as the
+// chunks land, and pass 2 from the staged copy.
 template <Op OP, typename T, int NT>
 __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowArgs a)
 {
@@ -86,12 +94,9 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kMaxChunks];
     __shared__ float2 red[NW];
-    __shared__ __align__(16) float4 part;  // this CTA's (a, b, failed): read by cluster peers
     __shared__ float4 fin;
 
-    const int C = a.C;
-    const int64_t row = blockIdx.x / C;
-    const int rank = C > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int64_t row = blockIdx.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
 
@@ -104,12 +109,10 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
     // Every operand of a row shares this geometry (the host checks that their
     // row starts agree modulo 16 bytes).
     const RowGeom g = row_geom(in0, a.cols);
-    const int64_t v0 = static_cast<int64_t>(rank) * a.per_vec;
-    const int64_t vend = v0 + a.per_vec < g.nvec ? v0 + a.per_vec : g.nvec;
-    const int cnt = vend > v0 ? static_cast<int>(vend - v0) : 0;
-    const int64_t body = g.head + v0 * VEC;  // column of this CTA's first vector
-    const bool head_here = rank == 0 && tid < g.head;
-    const bool tail_here = rank == C - 1 && tid < g.tail;
+    const int cnt = static_cast<int>(g.nvec);
+    const bool head_here = tid < g.head;
+    const bool tail_here = tid < g.tail;
+    uint4 *o = reinterpret_cast<uint4 *>(out + g.head);
 
     int64_t y = -1;
     if constexpr (OP == Op::CE) {
@@ -117,20 +120,19 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
         if (y == a.ignore_index) {
             // ignored row: zero gradient, zero loss, nothing read
             const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            uint4 *o = reinterpret_cast<uint4 *>(out + body);
             for (int j = tid; j < cnt; j += NT)
                 __stcs(o + j, z);
             if (head_here)
                 E::store(out + tid, 0.f);
             if (tail_here)
                 E::store(out + g.tail_start + tid, 0.f);
-            if (rank == 0 && tid == 0)
+            if (tid == 0)
                 a.row_loss[row] = 0.f;
             return;
         }
         if (y < 0 || y >= a.cols) {
             // out-of-range target: flag it, NaN loss, leave the row as it is
-            if (rank == 0 && tid == 0) {
+            if (tid == 0) {
                 a.row_loss[row] = __int_as_float(0x7fc00000);
                 atomicOr(&g_flags, kFlagBadTarget);
             }
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
         }
     }
 
-    // ---- issue the bulk copies of this CTA's slice (one mbarrier per chunk)
+    // ---- issue the bulk copies of the row (one mbarrier per chunk)
     const int nch = cnt ? (cnt + a.chunk_vec - 1) / a.chunk_vec : 0;
     const uint32_t buf0 = smem_addr(smem);
     const uint32_t buf1 = buf0 + static_cast<uint32_t>(a.per_vec) * 16u;
@@ -156,9 +158,10 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
             const uint32_t bytes = static_cast<uint32_t>(c1 - c0) * 16u;
             const uint32_t bar = smem_addr(&bars[k]);
             mbar_arrive_expect_tx(bar, bytes * NBUF);
-            bulk_load(buf0 + c0 * 16u, in0 + body + static_cast<int64_t>(c0) * VEC, bytes, bar, pol);
+            bulk_load(buf0 + c0 * 16u, in0 + g.head + static_cast<int64_t>(c0) * VEC, bytes, bar,
+                      pol);
             if constexpr (NBUF == 2)
-                bulk_load(buf1 + c0 * 16u, in1 + body + static_cast<int64_t>(c0) * VEC, bytes, bar,
+                bulk_load(buf1 + c0 * 16u, in1 + g.head + static_cast<int64_t>(c0) * VEC, bytes, bar,
                           pol);
         }
     }
@@ -175,9 +178,9 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
         if constexpr (NBUF == 2)
             t1 = E::load(in1 + g.tail_start + tid);
     }
-    float xy = 0.f;  // the target logit, read before this cluster stores anything
+    float xy = 0.f;  // the target logit, read before this CTA stores anything
     if constexpr (OP == Op::CE) {
-        if (rank == 0 && tid == 0)
+        if (tid == 0)
             xy = E::load(in0 + y);
     }
 
@@ -185,11 +188,11 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
     bool ok = true;
     float pa, pb;  // (m, d) for CE / softmax fwd, (sum y*dy, unused) for softmax bwd
     if constexpr (OP == Op::SoftmaxBwd) {
-        float s = 0.f;
+        float sdot = 0.f;
         if (head_here)
-            s = fmaf(h0, h1, s);
+            sdot = fmaf(h0, h1, sdot);
         if (tail_here)
-            s = fmaf(t0, t1, s);
+            sdot = fmaf(t0, t1, sdot);
         for (int k = 0; k < nch && ok; ++k) {
             ok = mbar_wait_bounded(smem_addr(&bars[k]), 0);
             const int c1 = (k + 1) * a.chunk_vec < cnt ? (k + 1) * a.chunk_vec : cnt;
@@ -200,11 +203,12 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
                     E::unpack(ld_shared_v4(buf1 + j * 16u), fd);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e)
-                        s = fmaf(fy[e], fd[e], s);
+                        sdot = fmaf(fy[e], fd[e], sdot);
                 }
             }
         }
-        pa = s;
+        ok = __syncthreads_and(ok);
+        pa = sdot;
         pb = 0.f;
     } else {
         float m = -INFINITY;
@@ -216,16 +220,29 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
             ok = mbar_wait_bounded(smem_addr(&bars[k]), 0);
             const int c1 = (k + 1) * a.chunk_vec < cnt ? (k + 1) * a.chunk_vec : cnt;
             if (ok) {
-                for (int j = k * a.chunk_vec + tid; j < c1; j += NT) {
-                    float f[VEC];
-                    E::unpack(ld_shared_v4(buf0 + j * 16u), f);
+                if constexpr (VEC == 8) {
+                    // bf16: packed max of element pairs, no unpacking
+                    __nv_bfloat162 mm = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+                    for (int j = k * a.chunk_vec + tid; j < c1; j += NT) {
+                        const uint4 v = ld_shared_v4(buf0 + j * 16u);
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e)
-                        m = fmaxf(m, f[e]);
+                        for (int e = 0; e < 4; ++e)
+                            mm = __hmax2(mm, *reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                    }
+                    m = fmaxf(m, fmaxf(__low2float(mm), __high2float(mm)));
+                } else {
+                    for (int j = k * a.chunk_vec + tid; j < c1; j += NT) {
+                        float f[VEC];
+                        E::unpack(ld_shared_v4(buf0 + j * 16u), f);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            m = fmaxf(m, f[e]);
+                    }
                 }
             }
         }
-        // every chunk has landed once the loop above completed for all threads
+        // every chunk has landed once all threads passed the loop above
         ok = __syncthreads_and(ok);
         float d = 0.f;
         if (ok) {
@@ -245,8 +262,6 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
         pa = m;
         pb = d;
     }
-    if constexpr (OP == Op::SoftmaxBwd)
-        ok = __syncthreads_and(ok);
 
     // ---- CTA reduction of the partials
     P::warp_reduce(pa, pb);
@@ -259,57 +274,28 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
         pb = lane < NW ? red[lane].y : e.y;
         P::warp_reduce(pa, pb);
         if (lane == 0)
-            part = make_float4(pa, pb, ok ? 0.f : 1.f, 0.f);
+            fin = make_float4(pa, pb, 0.f, 0.f);
     }
     __syncthreads();
-
-    // ---- cluster reduction over distributed shared memory
-    float4 r;
-    if (C > 1) {
-        cluster_arrive();
-        cluster_wait();  // every CTA's `part` is now visible
-        if (warp == 0) {
-            const float2 e = P::empty();
-            float qa = e.x, qb = e.y, qf = 0.f;
-            if (lane < C) {
-                const uint32_t peer = map_to_rank(smem_addr(&part), static_cast<uint32_t>(lane));
-                const float2 ab = ld_cluster_f2(peer);
-                const float2 fl = ld_cluster_f2(peer + 8u);
-                qa = ab.x;
-                qb = ab.y;
-                qf = fl.x;
-            }
-            P::warp_reduce(qa, qb);
-            qf = warp_sum(qf);
-            if (lane == 0)
-                fin = make_float4(qa, qb, qf, 0.f);
-        }
-        cluster_arrive();  // done reading peers; the matching wait precedes exit
-        __syncthreads();
-        r = fin;
-    } else {
-        r = part;
-    }
-    const bool all_ok = r.z == 0.f;
+    const float4 r = fin;
 
     // ---- pass 2: results from the staged copy, one store per element
-    if (all_ok) {
-        uint4 *o = reinterpret_cast<uint4 *>(out + body);
+    if (ok) {
         if constexpr (OP == Op::SoftmaxBwd) {
-            const float s = r.x;
+            const float sdot = r.x;
             for (int j = tid; j < cnt; j += NT) {
                 float fy[VEC], fd[VEC];
                 E::unpack(ld_shared_v4(buf0 + j * 16u), fy);
                 E::unpack(ld_shared_v4(buf1 + j * 16u), fd);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    fy[e] = fy[e] * (fd[e] - s);
+                    fy[e] = fy[e] * (fd[e] - sdot);
                 __stcs(o + j, E::pack(fy));
             }
             if (head_here)
-                E::store(out + tid, h0 * (h1 - s));
+                E::store(out + tid, h0 * (h1 - sdot));
             if (tail_here)
-                E::store(out + g.tail_start + tid, t0 * (t1 - s));
+                E::store(out + g.tail_start + tid, t0 * (t1 - sdot));
         } else {
             const float M = r.x, D = r.y;
             const float ML = M * kLog2e;
@@ -321,7 +307,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
             } else {
                 scale = 1.f / D;
             }
-            const int64_t ycol = y - body;  // target position relative to this slice
+            const int64_t ycol = y - g.head;  // target position relative to the vectors
             for (int j = tid; j < cnt; j += NT) {
                 float f[VEC];
                 E::unpack(ld_shared_v4(buf0 + j * 16u), f);
@@ -354,24 +340,531 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
                                                                     : ex * scale);
             }
             if constexpr (OP == Op::CE) {
-                if (rank == 0 && tid == 0)
+                if (tid == 0)
                     a.row_loss[row] = M + logf(D) - xy;
             }
         }
     } else {
         if (tid == 0) {
             atomicOr(&g_flags, kFlagTimeout);
+            if constexpr (OP == Op::CE)
+                a.row_loss[row] = __int_as_float(0x7fc00000);
             // give copies still in flight a bounded chance to land before exit
             for (int k = 0; k < nch; ++k)
                 mbar_wait_bounded(smem_addr(&bars[k]), 0);
         }
-        if constexpr (OP == Op::CE) {
-            if (rank == 0 && tid == 0)
-                a.row_loss[row] = __int_as_float(0x7fc00000);
+    }
+}
+
+// ---------------------------------------------------------------------------
+template <Op OP>
+__device__ __forceinline__ bool row_is_live(const RowArgs &a, int64_t y)
+{
+    if constexpr (OP == Op::CE)
+        return y != a.ignore_index && y >= 0 && y < a.cols;
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Warp-specialised ring form (one CTA per row, persistent over rows).
+//
+// A producer warp streams each live row through a ring of shared-memory
+// chunks with 1-D bulk copies: first the whole row for pass 1, then the row
+// again, chunks in reverse order, for pass 2.  The consumer warps reduce the
+// pass-1 chunks online, merge (m, d) across the CTA, and write the pass-2
+// results.  The ring keeps up to its whole capacity of loads in flight
+// through every phase (including the reduction), and the second read of a
+// row follows the first by one row-time, so it is served by L2: HBM sees one
+// read and one write per element, as with a row held on chip, without
+// splitting rows across SMs.  full[s] (count 1 + bytes) and empty[s] (one
+// arrival per consumer warp) hand each slot back and forth; every wait is
+// bounded.
+__device__ __forceinline__ void named_barrier_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// L2 policy for data that will be read again soon.
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+constexpr int kRingMaxSlots = 32;
+
+constexpr int kRingMaxCluster = 16;
+
+template <Op OP, typename T, int NCW, int VPT>
+__global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowArgs a)
+{
+    using E = Elem<T>;
+    using P = Partial<OP>;
+    constexpr int VEC = E::kPerVec;
+    constexpr int NBUF = (OP == Op::SoftmaxBwd) ? 2 : 1;
+    constexpr int NC = NCW * 32;            // consumer threads
+    constexpr int CHUNK = NC * VPT;         // 16-byte vectors per ring slot and operand
+    constexpr uint32_t kChunkBytes = CHUNK * 16u;
+    constexpr uint32_t kSlotBytes = kChunkBytes * NBUF;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[kRingMaxSlots];
+    __shared__ __align__(8) uint64_t empty[kRingMaxSlots];
+    __shared__ __align__(8) uint64_t xbar[2];  // cluster exchange, by live-row parity
+    __shared__ __align__(16) float4 xslot[2][kRingMaxCluster];
+    __shared__ float2 red[NCW];
+    __shared__ float4 fin;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int C = a.C;
+    const int rank = C > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int64_t cid = blockIdx.x / C;
+    const int64_t G = gridDim.x / C;
+    const int nslot = a.nslot;
+    const uint32_t ring = smem_addr(smem);
+
+    if (tid == 0) {
+        for (int s = 0; s < nslot; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), NCW);
+        }
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (C > 1) {  // every peer's barriers exist before anyone signals them
+        cluster_arrive_any();
+        cluster_wait_any();
+    }
+
+    if (warp == NCW) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
+            uint32_t slot = 0, ph = 0;
+            bool ok = true;
+            int64_t ynext = (OP == Op::CE && cid < a.M) ? a.targets[cid] : 0;
+            for (int64_t row = cid; row < a.M && ok; row += G) {
+                const int64_t y = ynext;
+                if (OP == Op::CE && row + G < a.M)
+                    ynext = a.targets[row + G];
+                if (!row_is_live<OP>(a, y))
+                    continue;  // ignored or invalid target: nothing to read
+                const T *in0 = static_cast<const T *>(a.in0) + row * a.s0;
+                const T *in1 = nullptr;
+                if constexpr (NBUF == 2)
+                    in1 = static_cast<const T *>(a.in1) + row * a.s1;
+                const RowGeom g = row_geom(in0, a.cols);
+                const int64_t per = (g.nvec + C - 1) / C;
+                const int64_t v0 = rank * per;
+                const int64_t cnt = v0 < g.nvec ? (v0 + per < g.nvec ? per : g.nvec - v0) : 0;
+                const int64_t body = g.head + v0 * VEC;
+                const int64_t nch = (cnt + CHUNK - 1) / CHUNK;
+                // a slice that fills at most half the ring stays resident for both passes
+                const int passes = 2 * nch <= nslot ? 1 : 2;
+                for (int pass = 0; pass < passes && ok; ++pass) {
+                    for (int64_t kk = 0; kk < nch; ++kk) {
+                        const int64_t k = pass == 0 ? kk : nch - 1 - kk;
+                        const int64_t c0 = k * CHUNK;
+                        const int64_t c1 = c0 + CHUNK < cnt ? c0 + CHUNK : cnt;
+                        const uint32_t bytes = static_cast<uint32_t>(c1 - c0) * 16u;
+                        if (!mbar_wait_bounded(smem_addr(&empty[slot]), ph ^ 1u)) {
+                            ok = false;
+                            atomicOr(&g_flags, kFlagTimeout);
+                            break;
+                        }
+                        const uint32_t fb = smem_addr(&full[slot]);
+                        const uint32_t dst = ring + slot * kSlotBytes;
+                        mbar_arrive_expect_tx(fb, bytes * NBUF);
+                        bulk_load(dst, in0 + body + c0 * VEC, bytes, fb, pass == 0 ? keep : stream);
+                        if constexpr (NBUF == 2)
+                            bulk_load(dst + kChunkBytes, in1 + body + c0 * VEC, bytes, fb,
+                                      pass == 0 ? keep : stream);
+                        if (++slot == static_cast<uint32_t>(nslot)) {
+                            slot = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        // Thread tid owns vectors tid + v * NC (v < VPT) of every chunk: VPT
+        // independent 128-bit shared loads per chunk, issued back to back.
+        uint32_t slot = 0, ph = 0, xph = 0;
+        int live = 0;
+        bool ok = true;
+        const float nf = OP == Op::CE ? static_cast<float>(*a.n_ptr) : 1.f;
+        int64_t ynext = (OP == Op::CE && cid < a.M) ? a.targets[cid] : 0;
+        for (int64_t row = cid; row < a.M; row += G) {
+            const int64_t y = ynext;  // loaded one row ahead
+            if (OP == Op::CE && row + G < a.M)
+                ynext = a.targets[row + G];
+            const T *in0 = static_cast<const T *>(a.in0) + row * a.s0;
+            const T *in1 = nullptr;
+            if constexpr (NBUF == 2)
+                in1 = static_cast<const T *>(a.in1) + row * a.s1;
+            T *out = static_cast<T *>(a.out) + row * a.so;
+            const RowGeom g = row_geom(in0, a.cols);
+            const int64_t per = (g.nvec + C - 1) / C;
+            const int64_t v0 = rank * per;
+            const int64_t cnt = v0 < g.nvec ? (v0 + per < g.nvec ? per : g.nvec - v0) : 0;
+            const int64_t body = g.head + v0 * VEC;
+            const bool head_here = rank == 0 && tid < g.head;
+            const bool tail_here = rank == C - 1 && tid < g.tail;
+            uint4 *o = reinterpret_cast<uint4 *>(out + body);
+            if constexpr (OP == Op::CE) {
+                if (y == a.ignore_index) {
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    for (int64_t j = tid; j < cnt; j += NC)
+                        __stcs(o + j, z);
+                    if (head_here)
+                        E::store(out + tid, 0.f);
+                    if (tail_here)
+                        E::store(out + g.tail_start + tid, 0.f);
+                    if (rank == 0 && tid == 0)
+                        a.row_loss[row] = 0.f;
+                    continue;
+                }
+                if (y < 0 || y >= a.cols) {
+                    if (rank == 0 && tid == 0) {
+                        a.row_loss[row] = __int_as_float(0x7fc00000);
+                        atomicOr(&g_flags, kFlagBadTarget);
+                    }
+                    continue;
+                }
+            }
+            const int64_t nch = (cnt + CHUNK - 1) / CHUNK;
+            const bool hold = 2 * nch <= nslot;  // loaded once, kept for pass 2
+            const uint32_t slot0 = slot, ph0 = ph;
+            float h0 = 0.f, h1 = 0.f, t0 = 0.f, t1 = 0.f;
+            if (head_here) {
+                h0 = E::load(in0 + tid);
+                if constexpr (NBUF == 2)
+                    h1 = E::load(in1 + tid);
+            }
+            if (tail_here) {
+                t0 = E::load(in0 + g.tail_start + tid);
+                if constexpr (NBUF == 2)
+                    t1 = E::load(in1 + g.tail_start + tid);
+            }
+            float xy = 0.f;
+            if constexpr (OP == Op::CE) {
+                if (rank == 0 && tid == 0)
+                    xy = E::load(in0 + y);  // completes before this row's partial is published
+            }
+
+            // ---- pass 1: online over the chunks as they arrive
+            float pa, pb;
+            if constexpr (OP == Op::SoftmaxBwd) {
+                float sdot = 0.f;
+                if (head_here)
+                    sdot = fmaf(h0, h1, sdot);
+                if (tail_here)
+                    sdot = fmaf(t0, t1, sdot);
+                for (int64_t kk = 0; kk < nch; ++kk) {
+                    const int64_t c0 = kk * CHUNK;
+                    const int cn = static_cast<int>((c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0);
+                    if (ok)
+                        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[slot]), ph));
+                    if (ok) {
+                        const uint32_t b0 = ring + slot * kSlotBytes;
+                        uint4 ry[VPT], rd[VPT];
+#pragma unroll
+                        for (int v = 0; v < VPT; ++v) {
+                            const int j = tid + v * NC;
+                            if (j < cn) {
+                                ry[v] = ld_shared_v4(b0 + j * 16u);
+                                rd[v] = ld_shared_v4(b0 + kChunkBytes + j * 16u);
+                            }
+                        }
+#pragma unroll
+                        for (int v = 0; v < VPT; ++v) {
+                            if (tid + v * NC < cn) {
+                                float fy[VEC], fd[VEC];
+                                E::unpack(ry[v], fy);
+                                E::unpack(rd[v], fd);
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e)
+                                    sdot = fmaf(fy[e], fd[e], sdot);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0 && ok && !hold)  // a warp that gave up stops releasing slots
+                        mbar_arrive(smem_addr(&empty[slot]));
+                    if (++slot == static_cast<uint32_t>(nslot)) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                }
+                pa = sdot;
+                pb = 0.f;
+            } else {
+                float m = -INFINITY, d = 0.f;
+                {
+                    float hm = -INFINITY;
+                    if (head_here)
+                        hm = h0;
+                    if (tail_here)
+                        hm = fmaxf(hm, t0);
+                    if (hm != -INFINITY) {
+                        m = hm;
+                        const float mL = m * kLog2e;
+                        if (head_here)
+                            d += exp2f(fmaf(h0, kLog2e, -mL));
+                        if (tail_here)
+                            d += exp2f(fmaf(t0, kLog2e, -mL));
+                    }
+                }
+                for (int64_t kk = 0; kk < nch; ++kk) {
+                    const int64_t c0 = kk * CHUNK;
+                    const int cn = static_cast<int>((c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0);
+                    if (ok)
+                        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[slot]), ph));
+                    if (ok) {
+                        const uint32_t b0 = ring + slot * kSlotBytes;
+                        uint4 raw[VPT];
+#pragma unroll
+                        for (int v = 0; v < VPT; ++v) {
+                            const int j = tid + v * NC;
+                            // a vector past the slice end reads as bf16 -inf pairs (fp32 skips it)
+                            raw[v] = j < cn ? ld_shared_v4(b0 + j * 16u)
+                                            : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u,
+                                                         0xff80ff80u);
+                        }
+                        // the chunk's max first (packed pairs for bf16), then one rescale and the sum
+                        float cm = -INFINITY;
+                        if constexpr (VEC == 8) {
+                            __nv_bfloat162 mm = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+#pragma unroll
+                            for (int v = 0; v < VPT; ++v) {
+                                const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    mm = __hmax2(mm, *reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                            }
+                            cm = fmaxf(__low2float(mm), __high2float(mm));
+                        } else {
+#pragma unroll
+                            for (int v = 0; v < VPT; ++v) {
+                                if (tid + v * NC < cn) {
+                                    float f[VEC];
+                                    E::unpack(raw[v], f);
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e)
+                                        cm = fmaxf(cm, f[e]);
+                                }
+                            }
+                        }
+                        const float mn = fmaxf(m, cm);
+                        if (mn != -INFINITY) {
+                            const float mL = mn * kLog2e;
+                            float s = 0.f;
+#pragma unroll
+                            for (int v = 0; v < VPT; ++v) {
+                                if (tid + v * NC < cn) {
+                                    float f[VEC];
+                                    E::unpack(raw[v], f);
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e)
+                                        s += exp2f(fmaf(f[e], kLog2e, -mL));
+                                }
+                            }
+                            d = d * exp2f((m - mn) * kLog2e) + s;
+                            m = mn;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0 && ok && !hold)
+                        mbar_arrive(smem_addr(&empty[slot]));
+                    if (++slot == static_cast<uint32_t>(nslot)) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                }
+                pa = m;
+                pb = d;
+            }
+
+            // ---- merge across the consumer warps
+            P::warp_reduce(pa, pb);
+            if (lane == 0)
+                red[warp] = make_float2(pa, pb);
+            named_barrier_sync(1, NC);
+            if (warp == 0) {
+                const float2 e = P::empty();
+                pa = lane < NCW ? red[lane].x : e.x;
+                pb = lane < NCW ? red[lane].y : e.y;
+                P::warp_reduce(pa, pb);
+                if (lane == 0)
+                    fin = make_float4(pa, pb, ok ? 0.f : 1.f, 0.f);
+            }
+            named_barrier_sync(1, NC);
+            float4 r = fin;
+
+            // ---- merge across the cluster: each CTA sends its partial to every
+            // peer's slot (st.async, counted on the peer's exchange barrier) and
+            // folds the C partials in rank order, so all CTAs get the same bits.
+            if (C > 1) {
+                const int pi = live & 1;
+                if (tid == 0) {
+                    asm volatile("" ::"f"(xy));  // the target logit was read before peers store
+                    mbar_arrive_expect_tx(smem_addr(&xbar[pi]), 16u * static_cast<uint32_t>(C - 1));
+                    const uint32_t slot_addr = smem_addr(&xslot[pi][rank]);
+                    const uint32_t bar_addr = smem_addr(&xbar[pi]);
+                    for (int q = 0; q < C; ++q)
+                        if (q != rank)
+                            st_async_f4(map_to_rank(slot_addr, q), r, map_to_rank(bar_addr, q));
+                }
+                bool xok = ok;
+                if (xok)
+                    xok = __all_sync(0xffffffffu,
+                                     mbar_wait_bounded(smem_addr(&xbar[pi]), (xph >> pi) & 1u));
+                xph ^= 1u << pi;
+                const float2 e = P::empty();
+                float qa = e.x, qb = e.y, qf = xok ? 0.f : 1.f;
+                for (int q = 0; q < C; ++q) {
+                    const float4 v = q == rank ? r : xslot[pi][q];
+                    P::merge(qa, qb, v.x, v.y);
+                    qf += v.z;
+                }
+                r = make_float4(qa, qb, qf, 0.f);
+                ok = ok && xok;
+            }
+            ++live;
+
+            // ---- pass 2: the slice again, chunks in reverse order
+            float scale = 0.f, sub = 0.f, ML = 0.f;
+            if constexpr (OP != Op::SoftmaxBwd) {
+                ML = r.x * kLog2e;
+                if constexpr (OP == Op::CE) {
+                    scale = 1.f / (r.y * nf);
+                    sub = 1.f / nf;
+                } else {
+                    scale = 1.f / r.y;
+                }
+            }
+            const bool all_ok = r.z == 0.f;
+            const int64_t ycol = y - body;
+            if (hold) {  // revisit the slots pass 1 read
+                slot = slot0;
+                ph = ph0;
+            }
+            for (int64_t kk = 0; kk < nch; ++kk) {
+                const int64_t k = hold ? kk : nch - 1 - kk;
+                const int64_t c0 = k * CHUNK;
+                const int cn = static_cast<int>((c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0);
+                if (ok && !hold)
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[slot]), ph));
+                if (ok && all_ok) {
+                    const uint32_t b0 = ring + slot * kSlotBytes;
+                    uint4 raw[VPT], raw2[VPT];
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) {
+                        const int j = tid + v * NC;
+                        if (j < cn) {
+                            raw[v] = ld_shared_v4(b0 + j * 16u);
+                            if constexpr (NBUF == 2)
+                                raw2[v] = ld_shared_v4(b0 + kChunkBytes + j * 16u);
+                        }
+                    }
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) {
+                        const int j = tid + v * NC;
+                        if (j >= cn)
+                            continue;
+                        const int64_t vj = c0 + j;  // vector index within the slice
+                        if constexpr (OP == Op::SoftmaxBwd) {
+                            float fy[VEC], fd[VEC];
+                            E::unpack(raw[v], fy);
+                            E::unpack(raw2[v], fd);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e)
+                                fy[e] = fy[e] * (fd[e] - r.x);
+                            __stcs(o + vj, E::pack(fy));
+                        } else {
+                            float f[VEC];
+                            E::unpack(raw[v], f);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e)
+                                f[e] = exp2f(fmaf(f[e], kLog2e, -ML));
+                            float gr[VEC];
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e)
+                                gr[e] = f[e] * scale;
+                            if constexpr (OP == Op::CE) {
+                                const int64_t rel = ycol - vj * VEC;
+                                if (rel >= 0 && rel < VEC) {  // the target column: (p_y - 1) / n
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e)
+                                        if (e == rel)
+                                            gr[e] = fmaf(f[e], scale, -sub);
+                                }
+                            }
+                            __stcs(o + vj, E::pack(gr));
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0 && ok)
+                    mbar_arrive(smem_addr(&empty[slot]));
+                if (++slot == static_cast<uint32_t>(nslot)) {
+                    slot = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (ok && all_ok) {
+                if constexpr (OP == Op::SoftmaxBwd) {
+                    if (head_here)
+                        E::store(out + tid, h0 * (h1 - r.x));
+                    if (tail_here)
+                        E::store(out + g.tail_start + tid, t0 * (t1 - r.x));
+                } else {
+                    if (head_here) {
+                        const float ex = exp2f(fmaf(h0, kLog2e, -ML));
+                        E::store(out + tid,
+                                 (OP == Op::CE && y == tid) ? fmaf(ex, scale, -sub) : ex * scale);
+                    }
+                    if (tail_here) {
+                        const float ex = exp2f(fmaf(t0, kLog2e, -ML));
+                        E::store(out + g.tail_start + tid,
+                                 (OP == Op::CE && y == g.tail_start + tid) ? fmaf(ex, scale, -sub)
+                                                                            : ex * scale);
+                    }
+                    if constexpr (OP == Op::CE) {
+                        if (rank == 0 && tid == 0)
+                            a.row_loss[row] = r.x + logf(r.y) - xy;
+                    }
+                }
+            } else if (tid == 0) {
+                atomicOr(&g_flags, kFlagTimeout);
+                if constexpr (OP == Op::CE) {
+                    if (rank == 0)
+                        a.row_loss[row] = __int_as_float(0x7fc00000);
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            // a wait gave up: linger (bounded) so copies still in flight land before exit
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < kWaitLimitNs / 10) {
+            }
         }
     }
-    if (C > 1)
-        cluster_wait();
+    if (C > 1) {  // no CTA leaves while a peer may still signal it
+        cluster_arrive_any();
+        cluster_wait_any();
+    }
 }
 
 // ---------------------------------------------------------------------------
