@@ -294,7 +294,11 @@ cudaError_t resident_clusters(KernelFn fn, const Plan &p, int device, int64_t *o
     return cudaSuccess;
 }
 
-cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a, cudaStream_t stream)
+// `after_count`: the row kernel follows ce_count_kernel on the stream and may
+// start while it runs (programmatic dependent launch); it waits for it on the
+// device before it reads n.
+cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a, cudaStream_t stream,
+                        bool after_count = false)
 {
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
@@ -317,15 +321,22 @@ cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a, cudaStream
     cfg.blockDim = dim3(static_cast<unsigned>(p.nt), 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned nattr = 0;
     if (p.C > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = static_cast<unsigned>(p.C);
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
     }
+    if (after_count) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    cfg.attrs = nattr ? attr : nullptr;
+    cfg.numAttrs = nattr;
     TimedRegion timed(stream);
     return cudaLaunchKernelEx(&cfg, fn, a);
 }
@@ -363,6 +374,55 @@ bool same_phase(const void *a, int64_t sa, const void *b, int64_t sb, size_t esi
     return ((sa - sb) * static_cast<int64_t>(esize)) % 16 == 0;
 }
 
+// Temporary storage of one cross-entropy call: [0, 4) the non-ignored count
+// n, [kCeScratchHeader, + 4 M) the row losses.
+constexpr size_t kCeScratchHeader = 256;
+
+// The cross-entropy launches on `stream`: the count kernel (n; the NaN mean
+// when M == 0), the row kernel, then the mean kernel, each of the last two
+// launched as a programmatic dependent of the one before.
+cudaError_t launch_ce(void *logits, int64_t stride, const int64_t *targets, float *loss, int64_t M,
+                      int64_t V, int64_t ignore_index, int dtype, void *scratch,
+                      cudaStream_t stream)
+{
+    int *n_ptr = static_cast<int *>(scratch);
+    float *row_loss = reinterpret_cast<float *>(static_cast<char *>(scratch) + kCeScratchHeader);
+    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr, loss);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || M == 0)
+        return e;
+    const Plan p = make_plan(V, elem_size(dtype), 1, true);
+    RowArgs a{};
+    a.in0 = logits;
+    a.s0 = stride;
+    a.out = logits;
+    a.so = stride;
+    a.M = M;
+    a.cols = V;
+    a.targets = targets;
+    a.ignore_index = ignore_index;
+    a.n_ptr = n_ptr;
+    a.row_loss = row_loss;
+    a.C = p.C;
+    a.per_vec = p.per_vec;
+    a.chunk_vec = p.chunk_vec;
+    a.nslot = p.nslot;
+    e = launch_rows(pick<Op::CE>(dtype, p), p, a, stream, true);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(1024, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ce_mean_kernel<1024>, static_cast<const float *>(row_loss), M,
+                              static_cast<const int *>(n_ptr), loss);
+}
+
 }  // namespace
 }  // namespace gbce
 
@@ -390,39 +450,11 @@ extern "C" int ce_fwd_bwd(void *logits, int64_t stride, const int64_t *targets, 
     cudaMemPool_t pool;
     if ((e = pool_for(device, &pool)) != cudaSuccess)
         return map_error(e);
-    // scratch: [0, 16) the non-ignored count; [256, 256 + 4M) the row losses
     void *scratch = nullptr;
-    const size_t bytes = 256 + static_cast<size_t>(M) * sizeof(float);
+    const size_t bytes = kCeScratchHeader + static_cast<size_t>(M) * sizeof(float);
     if ((e = cudaMallocFromPoolAsync(&scratch, bytes, pool, stream)) != cudaSuccess)
         return map_error(e);
-    int *n_ptr = static_cast<int *>(scratch);
-    float *row_loss = reinterpret_cast<float *>(static_cast<char *>(scratch) + 256);
-
-    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr);
-    e = cudaGetLastError();
-    if (e == cudaSuccess && M > 0) {
-        const Plan p = make_plan(V, elem_size(dtype), 1, true);
-        RowArgs a{};
-        a.in0 = logits;
-        a.s0 = stride;
-        a.out = logits;
-        a.so = stride;
-        a.M = M;
-        a.cols = V;
-        a.targets = targets;
-        a.ignore_index = ignore_index;
-        a.n_ptr = n_ptr;
-        a.row_loss = row_loss;
-        a.C = p.C;
-        a.per_vec = p.per_vec;
-        a.chunk_vec = p.chunk_vec;
-        a.nslot = p.nslot;
-        e = launch_rows(pick<Op::CE>(dtype, p), p, a, stream);
-    }
-    if (e == cudaSuccess) {
-        ce_mean_kernel<1024><<<1, 1024, 0, stream>>>(row_loss, M, n_ptr, loss);
-        e = cudaGetLastError();
-    }
+    e = launch_ce(logits, stride, targets, loss, M, V, ignore_index, dtype, scratch, stream);
     cudaError_t ef = cudaFreeAsync(scratch, stream);
     if (e == cudaSuccess)
         e = ef;
@@ -573,11 +605,10 @@ namespace gbce {
 namespace {
 
 constexpr int64_t kNoAllocMaxRows = GBCE_NOALLOC_MAX_ROWS;
-constexpr size_t kNoAllocHeader = 256;  // [0, 4): the non-ignored count
-
-// [0, 256): header; [256, 256 + 4 * kNoAllocMaxRows): the row losses.
+// Laid out like the pool scratch of ce_fwd_bwd: the count, then
+// kNoAllocMaxRows row losses.
 static __device__ __align__(256) unsigned char
-    g_noalloc_scratch[kNoAllocHeader + kNoAllocMaxRows * sizeof(float)];
+    g_noalloc_scratch[kCeScratchHeader + kNoAllocMaxRows * sizeof(float)];
 
 std::mutex g_noalloc_mu;
 void *g_noalloc_addr[kMaxDevices] = {};
@@ -629,34 +660,8 @@ extern "C" int ce_fwd_bwd_noalloc(void *logits, int64_t stride, const int64_t *t
     if ((e = noalloc_scratch(device, &scratch)) != cudaSuccess)
         return map_error(e);
     // ce_count_kernel overwrites the count and the row kernel writes the loss
-    // of every row 0..M-1 before ce_mean_kernel reads it: nothing needs clearing.
-    int *n_ptr = static_cast<int *>(scratch);
-    float *row_loss = reinterpret_cast<float *>(static_cast<char *>(scratch) + kNoAllocHeader);
-
-    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr);
-    e = cudaGetLastError();
-    if (e == cudaSuccess && M > 0) {
-        const Plan p = make_plan(V, elem_size(dtype), 1, true);
-        RowArgs a{};
-        a.in0 = logits;
-        a.s0 = stride;
-        a.out = logits;
-        a.so = stride;
-        a.M = M;
-        a.cols = V;
-        a.targets = targets;
-        a.ignore_index = ignore_index;
-        a.n_ptr = n_ptr;
-        a.row_loss = row_loss;
-        a.C = p.C;
-        a.per_vec = p.per_vec;
-        a.chunk_vec = p.chunk_vec;
-        a.nslot = p.nslot;
-        e = launch_rows(pick<Op::CE>(dtype, p), p, a, stream);
-    }
-    if (e == cudaSuccess) {
-        ce_mean_kernel<1024><<<1, 1024, 0, stream>>>(row_loss, M, n_ptr, loss);
-        e = cudaGetLastError();
-    }
+    // of every row 0..M-1 before the mean kernel reads them: nothing left by
+    // an earlier call is read.
+    e = launch_ce(logits, stride, targets, loss, M, V, ignore_index, dtype, scratch, stream);
     return map_error(e);
 }

@@ -77,6 +77,61 @@ struct Partial {
     }
 };
 
+__device__ __forceinline__ void named_barrier_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Wait for the kernel this one depends on (launched before it with
+// programmatic stream serialisation) to complete and publish its writes.
+__device__ __forceinline__ void wait_prerequisite_grid()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// sum_{r < M} row_loss[r] in fp64 by NTH threads (tid < NTH, all calling,
+// synchronised by named barrier `bar`), in a fixed order: thread t adds the
+// 16-byte groups t, t + NTH, ... (each group's four values in order), then
+// fixed warp butterflies, so the same inputs give the same bits.  Returns the
+// total in thread 0.  row_loss is 16-byte aligned.  Loads go through L2.
+template <int NTH>
+__device__ __forceinline__ double sum_row_losses(const float *row_loss, int64_t M, int tid, int bar)
+{
+    __shared__ double part[NTH / 32];
+    const float4 *v = reinterpret_cast<const float4 *>(row_loss);
+    const int64_t nv = M / 4;
+    double s = 0.0;
+    int64_t i = tid;
+    for (; i + 3 * NTH < nv; i += 4 * NTH) {  // four independent 16-byte loads in flight
+        const float4 a = __ldcg(v + i), b = __ldcg(v + i + NTH);
+        const float4 c = __ldcg(v + i + 2 * NTH), d = __ldcg(v + i + 3 * NTH);
+        s += static_cast<double>(a.x) + a.y + a.z + a.w;
+        s += static_cast<double>(b.x) + b.y + b.z + b.w;
+        s += static_cast<double>(c.x) + c.y + c.z + c.w;
+        s += static_cast<double>(d.x) + d.y + d.z + d.w;
+    }
+    for (; i < nv; i += NTH) {
+        const float4 a = __ldcg(v + i);
+        s += static_cast<double>(a.x) + a.y + a.z + a.w;
+    }
+    if (tid == 0)
+        for (int64_t j = nv * 4; j < M; ++j)
+            s += static_cast<double>(__ldcg(row_loss + j));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        s += __shfl_xor_sync(0xffffffffu, s, off);
+    if ((tid & 31) == 0)
+        part[tid >> 5] = s;
+    named_barrier_sync(bar, NTH);
+    if (tid < 32) {
+        s = tid < NTH / 32 ? part[tid] : 0.0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, off);
+    }
+    return s;
+}
+
 // ---------------------------------------------------------------------------
 // Resident form, for rows whose operands fit one CTA's shared memory (<= 64 KB
 // per row in all): one CTA per row, three CTAs per SM.  The CTA stages its row
@@ -99,6 +154,8 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
+    if constexpr (OP == Op::CE)  // the mean kernel may be scheduled (it waits for this grid)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const T *in0 = static_cast<const T *>(a.in0) + row * a.s0;
     const T *in1 = nullptr;
@@ -301,6 +358,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
             const float ML = M * kLog2e;
             float scale, sub = 0.f;
             if constexpr (OP == Op::CE) {
+                wait_prerequisite_grid();  // n comes from the count kernel
                 const float n = static_cast<float>(*a.n_ptr);
                 scale = 1.f / (D * n);
                 sub = 1.f / n;
@@ -379,11 +437,6 @@ __device__ __forceinline__ bool row_is_live(const RowArgs &a, int64_t y)
 // splitting rows across SMs.  full[s] (count 1 + bytes) and empty[s] (one
 // arrival per consumer warp) hand each slot back and forth; every wait is
 // bounded.
-__device__ __forceinline__ void named_barrier_sync(int id, int threads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -503,6 +556,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
         uint32_t slot = 0, ph = 0, xph = 0;
         int live = 0;
         bool ok = true;
+        if constexpr (OP == Op::CE) {
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            wait_prerequisite_grid();  // n comes from the count kernel
+        }
         const float nf = OP == Op::CE ? static_cast<float>(*a.n_ptr) : 1.f;
         int64_t ynext = (OP == Op::CE && cid < a.M) ? a.targets[cid] : 0;
         for (int64_t row = cid; row < a.M; row += G) {
@@ -886,6 +943,8 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
     const int64_t row = blockIdx.x / C;
     const int rank = C > 1 ? static_cast<int>(cluster_rank()) : 0;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if constexpr (OP == Op::CE)  // the mean kernel may be scheduled (it waits for this grid)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const T *in0 = static_cast<const T *>(a.in0) + row * a.s0;
     const T *in1 = OP == Op::SoftmaxBwd ? static_cast<const T *>(a.in1) + row * a.s1 : nullptr;
     T *out = static_cast<T *>(a.out) + row * a.so;
@@ -979,6 +1038,7 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
         const float ML = r.x * kLog2e;
         float scale, sub = 0.f;
         if constexpr (OP == Op::CE) {
+            wait_prerequisite_grid();  // n comes from the count kernel
             const float n = static_cast<float>(*a.n_ptr);
             scale = 1.f / (r.y * n);
             sub = 1.f / n;
@@ -1001,18 +1061,24 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// n = number of targets != ignore_index (one CTA); flags targets outside [0, V).
+// n = number of targets != ignore_index (one CTA); flags targets outside [0, V);
+// for M == 0 writes the mean 0/0 = NaN itself.  It lets the row kernel launch
+// at once (programmatic dependent launch); the row kernel waits for it on the
+// device before it reads n.
 template <int NT>
 __global__ void __launch_bounds__(NT) ce_count_kernel(const int64_t *targets, int64_t M, int64_t V,
-                                                      int64_t ignore_index, int *n_out)
+                                                      int64_t ignore_index, int *n_out,
+                                                      float *loss)
 {
     __shared__ int warp_n[NT / 32];
     __shared__ int any_bad;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0)
         any_bad = 0;
     __syncthreads();
     int n = 0;
     bool bad = false;
+#pragma unroll 4
     for (int64_t i = threadIdx.x; i < M; i += NT) {
         const int64_t y = targets[i];
         if (y != ignore_index) {
@@ -1035,31 +1101,24 @@ __global__ void __launch_bounds__(NT) ce_count_kernel(const int64_t *targets, in
             n += __shfl_xor_sync(0xffffffffu, n, off);
         if (threadIdx.x == 0) {
             *n_out = n;
+            if (M == 0)
+                *loss = __int_as_float(0x7fc00000);
             if (any_bad)
                 atomicOr(&g_flags, kFlagBadTarget);
         }
     }
 }
 
-// L = sum_r row_loss[r] / n, summed in fp64 in a fixed order (deterministic).
+// L = sum_r row_loss[r] / n after the row kernel (one CTA; launched as its
+// programmatic dependent, it waits for the row kernel to complete first).
 template <int NT>
 __global__ void __launch_bounds__(NT) ce_mean_kernel(const float *row_loss, int64_t M,
                                                      const int *n_ptr, float *loss)
 {
-    __shared__ double part[NT];
-    double s = 0.0;
-    for (int64_t i = threadIdx.x; i < M; i += NT)
-        s += static_cast<double>(row_loss[i]);
-    part[threadIdx.x] = s;
-    __syncthreads();
-#pragma unroll
-    for (int w = NT / 2; w > 0; w >>= 1) {
-        if (threadIdx.x < w)
-            part[threadIdx.x] += part[threadIdx.x + w];
-        __syncthreads();
-    }
+    wait_prerequisite_grid();
+    const double s = sum_row_losses<NT>(row_loss, M, threadIdx.x, 1);
     if (threadIdx.x == 0)
-        *loss = static_cast<float>(part[0] / static_cast<double>(*n_ptr));
+        *loss = static_cast<float>(s / static_cast<double>(__ldcg(n_ptr)));
 }
 
 }  // namespace gbce
