@@ -414,6 +414,60 @@ def run_gbce(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_table(args, local):
+    """--table: kernel-only time of every workload (one JSON line per entry)."""
+    import cross_entropy_loss_ce_gb300 as gbce
+    gbce.load_library()
+    torch.cuda.set_device(local)
+    peak, _ = measured_peaks()
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    steps = max(args.steps // 4, 10)
+
+    def kernel_ms(call, restore=None):
+        for _ in range(args.warmup):
+            if restore:
+                restore()
+            call()
+        torch.cuda.synchronize()
+        gbce.timing_read()
+        gbce.timing_enable(True)
+        for _ in range(steps):
+            if restore:
+                restore()
+            flush_l2(flush)
+            call()
+        torch.cuda.synchronize()
+        ms, n = gbce.timing_read()
+        gbce.timing_enable(False)
+        if gbce.last_error() != gbce.OK:
+            raise RuntimeError("device error flag raised")
+        return ms / max(n, 1)
+
+    for w in workloads.CE_WORKLOADS.values():
+        xd0, td = workloads.make_ce_inputs(w, "cuda")
+        xd = torch.empty_like(xd0)
+        loss = torch.empty((), dtype=torch.float32, device="cuda")
+        ms = kernel_ms(lambda: gbce.ce_fwd_bwd(xd, td, workloads.IGNORE_INDEX, loss),
+                       lambda: xd.copy_(xd0))
+        alg = ce_algorithmic_bytes(w, td.cpu().numpy())
+        print(json.dumps({"table": w.name, "kernel_us": 1e3 * ms, "rows_per_s": w.M / (ms / 1e3),
+                          "alg_gbs": alg / (ms / 1e3) / 1e9,
+                          "frac_of_measured_peak": alg / (ms / 1e3) / 1e9 / peak}), flush=True)
+        del xd0, xd
+        torch.cuda.empty_cache()
+    M = workloads.SOFTMAX_M
+    for N in workloads.SOFTMAX_NS:
+        x, y, dy = workloads.make_softmax_inputs(M, N, device="cuda")
+        out = torch.empty_like(x)
+        for name, call, nb in (("fwd", lambda: gbce.softmax_fwd(x, out), 2),
+                               ("bwd", lambda: gbce.softmax_bwd(y, dy, out), 3)):
+            ms = kernel_ms(call)
+            b = nb * M * N * 4
+            print(json.dumps({"table": f"softmax_{name}_f32_{M}x{N}", "kernel_us": 1e3 * ms,
+                              "rows_per_s": M / (ms / 1e3), "alg_gbs": b / (ms / 1e3) / 1e9,
+                              "frac_of_measured_peak": b / (ms / 1e3) / 1e9 / peak}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -428,6 +482,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-softmax", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--table", action="store_true",
+                    help="print the kernel time of every workload instead of the benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -440,6 +496,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, ws, rank)
+        elif args.table:
+            run_table(args, local)
         else:
             run_gbce(args, ws, rank, local)
     finally:

@@ -76,7 +76,7 @@ def test_ce_deterministic():
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("V", [1, 2, 3, 7, 8, 9, 33, 1000, 4099, 65537, 262147, 1000003])
+@pytest.mark.parametrize("V", [1, 2, 3, 7, 8, 9, 33, 1000, 4099, 20000, 40000, 65537, 262147, 1000003])
 def test_ce_shapes_padded_and_misaligned(dtype, V):
     """Ragged V (cluster sizes 1..16 and the streaming fallback), a padded row
     stride whose padding must stay untouched, and a base pointer off the
