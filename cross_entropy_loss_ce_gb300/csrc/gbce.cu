@@ -18,6 +18,7 @@ namespace gbce {
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kWarpMaxVpl = 8;                // rows of <= 32 * 8 16-byte vectors: warp kernel
 constexpr int64_t kResidentMax = 64 * 1024;   // rows up to this many staged bytes: resident kernel
 constexpr int64_t kSliceMax = 200 * 1024;     // dynamic shared memory limit set on every kernel
 constexpr int kMaxCluster = 16;
@@ -52,10 +53,11 @@ int64_t current_sm_count()
 // ---------------------------------------------------------------------------
 // launch plan: the kernel regime is chosen by the row length
 
-enum class Kind { Resident, Ring, Streaming };
+enum class Kind { Warp, Resident, Ring, Streaming };
 
 struct Plan {
     Kind kind;
+    int vpl;        // warp: 16-byte vectors per lane
     int C;          // CTAs per row = cluster size
     int nt;         // threads per CTA
     int per_vec;    // resident: 16-byte vectors staged per operand
@@ -80,6 +82,16 @@ Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned)
         return p;
     }
     const int64_t nvec = row_bytes / 16;  // >= whole vectors of any row
+    if (nvec <= 32 * kWarpMaxVpl) {
+        // very short rows: one warp per row, the row in registers
+        p.kind = Kind::Warp;
+        p.C = 1;
+        p.nt = kWarpRowsPerCta * 32;
+        p.vpl = 1;
+        while (32 * p.vpl < nvec)
+            p.vpl *= 2;
+        return p;
+    }
     if (nvec * 16 * nbuf <= kResidentMax) {
         // short rows: one CTA per row holds the row, three CTAs per SM
         p.kind = Kind::Resident;
@@ -120,6 +132,13 @@ template <Op OP, typename T>
 KernelFn pick_kernel(const Plan &p)
 {
     switch (p.kind) {
+    case Kind::Warp:
+        switch (p.vpl) {
+        case 1: return rows_warp_kernel<OP, T, 1>;
+        case 2: return rows_warp_kernel<OP, T, 2>;
+        case 4: return rows_warp_kernel<OP, T, 4>;
+        default: return rows_warp_kernel<OP, T, 8>;
+        }
     case Kind::Resident:
         return p.nt == 128 ? rows_resident_kernel<OP, T, 128> : rows_resident_kernel<OP, T, 256>;
     case Kind::Ring:
@@ -310,6 +329,8 @@ cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a, cudaStream
     if (e != cudaSuccess)
         return e;
     int64_t clusters = a.M;  // resident and streaming kernels: one CTA / cluster per row
+    if (p.kind == Kind::Warp)
+        clusters = (a.M + kWarpRowsPerCta - 1) / kWarpRowsPerCta;
     if (p.kind == Kind::Ring) {
         int64_t fit = 0;
         if ((e = resident_clusters(fn, p, device, &fit)) != cudaSuccess)

@@ -145,6 +145,229 @@ __device__ __forceinline__ float sum_row_losses(const float *row_loss, int64_t M
 }
 
 // ---------------------------------------------------------------------------
+// Warp form, for short rows (at most 32 * VPL 16-byte vectors per operand):
+// one warp per row, eight rows per CTA.  Each lane holds VPL vectors of its
+// row in registers (128-bit loads straight from global memory), the row's
+// reductions are warp shuffles, and pass 2 works from the registers: one read
+// and one write per element, no shared memory and no CTA barrier.
+constexpr int kWarpRowsPerCta = 8;
+
+template <Op OP, typename T, int VPL>
+__global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const RowArgs a)
+{
+    using E = Elem<T>;
+    constexpr int VEC = E::kPerVec;
+    constexpr int NBUF = (OP == Op::SoftmaxBwd) ? 2 : 1;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpRowsPerCta + (threadIdx.x >> 5);
+    if (OP == Op::CE && threadIdx.x == 0)  // the mean kernel may be scheduled (it waits for this grid)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (row >= a.M)
+        return;
+
+    const T *in0 = static_cast<const T *>(a.in0) + row * a.s0;
+    const T *in1 = nullptr;
+    if constexpr (NBUF == 2)
+        in1 = static_cast<const T *>(a.in1) + row * a.s1;
+    T *out = static_cast<T *>(a.out) + row * a.so;
+    const RowGeom g = row_geom(in0, a.cols);
+    const int cnt = static_cast<int>(g.nvec);
+    const bool head_here = lane < g.head;
+    const bool tail_here = lane < g.tail;
+    const uint4 *src0 = reinterpret_cast<const uint4 *>(in0 + g.head);
+    uint4 *o = reinterpret_cast<uint4 *>(out + g.head);
+
+    int64_t y = -1;
+    if constexpr (OP == Op::CE) {
+        y = a.targets[row];
+        if (y == a.ignore_index) {
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+                if (lane + 32 * v < cnt)
+                    __stcs(o + lane + 32 * v, z);
+            if (head_here)
+                E::store(out + lane, 0.f);
+            if (tail_here)
+                E::store(out + g.tail_start + lane, 0.f);
+            if (lane == 0)
+                a.row_loss[row] = 0.f;
+            return;
+        }
+        if (y < 0 || y >= a.cols) {
+            if (lane == 0) {
+                a.row_loss[row] = __int_as_float(0x7fc00000);
+                atomicOr(&g_flags, kFlagBadTarget);
+            }
+            return;
+        }
+    }
+
+    // the row, straight into registers
+    uint4 r0[VPL], r1[VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+        const int j = lane + 32 * v;
+        r0[v] = j < cnt ? __ldcs(src0 + j) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+        if constexpr (NBUF == 2)
+            r1[v] = j < cnt ? __ldcs(reinterpret_cast<const uint4 *>(in1 + g.head) + j)
+                            : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float h0 = 0.f, h1 = 0.f, t0 = 0.f, t1 = 0.f;
+    if (head_here) {
+        h0 = E::load(in0 + lane);
+        if constexpr (NBUF == 2)
+            h1 = E::load(in1 + lane);
+    }
+    if (tail_here) {
+        t0 = E::load(in0 + g.tail_start + lane);
+        if constexpr (NBUF == 2)
+            t1 = E::load(in1 + g.tail_start + lane);
+    }
+
+    if constexpr (OP == Op::SoftmaxBwd) {
+        float sdot = 0.f;
+        if (head_here)
+            sdot = fmaf(h0, h1, sdot);
+        if (tail_here)
+            sdot = fmaf(t0, t1, sdot);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            if (lane + 32 * v < cnt) {
+                float fy[VEC], fd[VEC];
+                E::unpack(r0[v], fy);
+                E::unpack(r1[v], fd);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    sdot = fmaf(fy[e], fd[e], sdot);
+            }
+        }
+        sdot = warp_sum(sdot);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            if (lane + 32 * v < cnt) {
+                float fy[VEC], fd[VEC];
+                E::unpack(r0[v], fy);
+                E::unpack(r1[v], fd);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    fy[e] = fy[e] * (fd[e] - sdot);
+                __stcs(o + lane + 32 * v, E::pack(fy));
+            }
+        }
+        if (head_here)
+            E::store(out + lane, h0 * (h1 - sdot));
+        if (tail_here)
+            E::store(out + g.tail_start + lane, t0 * (t1 - sdot));
+        return;
+    } else {
+        // the row maximum (vectors past the end read as -inf), then the normaliser
+        float m = -INFINITY;
+        if (head_here)
+            m = h0;
+        if (tail_here)
+            m = fmaxf(m, t0);
+        if constexpr (VEC == 8) {
+            __nv_bfloat162 mm = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                const uint32_t w[4] = {r0[v].x, r0[v].y, r0[v].z, r0[v].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    mm = __hmax2(mm, *reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+            }
+            m = fmaxf(m, fmaxf(__low2float(mm), __high2float(mm)));
+        } else {
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                if (lane + 32 * v < cnt) {
+                    float f[VEC];
+                    E::unpack(r0[v], f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e)
+                        m = fmaxf(m, f[e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const float ML = (m == -INFINITY) ? 0.f : m * kLog2e;
+        float d = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            if (lane + 32 * v < cnt) {
+                float f[VEC];
+                E::unpack(r0[v], f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    d += exp2f(fmaf(f[e], kLog2e, -ML));
+            }
+        }
+        if (head_here)
+            d += exp2f(fmaf(h0, kLog2e, -ML));
+        if (tail_here)
+            d += exp2f(fmaf(t0, kLog2e, -ML));
+        d = warp_sum(d);
+
+        float scale, sub = 0.f;
+        if constexpr (OP == Op::CE) {
+            wait_prerequisite_grid();  // n comes from the count kernel
+            const float n = static_cast<float>(*a.n_ptr);
+            scale = 1.f / (d * n);
+            sub = 1.f / n;
+        } else {
+            scale = 1.f / d;
+        }
+        const int64_t ycol = y - g.head;
+        float xy = 0.f;  // the target logit, from the registers of the lane that holds it
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            const int j = lane + 32 * v;
+            if (j < cnt) {
+                float f[VEC];
+                E::unpack(r0[v], f);
+                float gr[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    gr[e] = exp2f(fmaf(f[e], kLog2e, -ML)) * scale;
+                if constexpr (OP == Op::CE) {
+                    const int64_t rel = ycol - static_cast<int64_t>(j) * VEC;
+                    if (rel >= 0 && rel < VEC) {  // the target column: (p_y - 1) / n
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            if (e == rel) {
+                                gr[e] = fmaf(exp2f(fmaf(f[e], kLog2e, -ML)), scale, -sub);
+                                xy = f[e];
+                            }
+                    }
+                }
+                __stcs(o + j, E::pack(gr));
+            }
+        }
+        if (head_here) {
+            const float ex = exp2f(fmaf(h0, kLog2e, -ML));
+            E::store(out + lane, (OP == Op::CE && y == lane) ? fmaf(ex, scale, -sub) : ex * scale);
+            if (OP == Op::CE && y == lane)
+                xy = h0;
+        }
+        if (tail_here) {
+            const float ex = exp2f(fmaf(t0, kLog2e, -ML));
+            const bool at_y = OP == Op::CE && y == g.tail_start + lane;
+            E::store(out + g.tail_start + lane, at_y ? fmaf(ex, scale, -sub) : ex * scale);
+            if (at_y)
+                xy = t0;
+        }
+        if constexpr (OP == Op::CE) {
+            // exactly one lane holds the target logit; the others contribute 0
+            xy = warp_sum(xy);
+            if (lane == 0)
+                a.row_loss[row] = m + logf(d) - xy;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Resident form, for rows whose operands fit one CTA's shared memory (<= 64 KB
 // per row in all): one CTA per row, three CTAs per SM.  The CTA stages its row
 // with up to kMaxChunks bulk copies (one mbarrier each), runs pass 1 as the
