@@ -6,8 +6,9 @@ binding never import it.  The arithmetic lives in ``oracle.c`` (plain C,
 double precision, the textbook definitions row by row); this module only
 marshals numpy arrays through ctypes.
 
-Inputs are numpy arrays: fp32 values as ``float32``, bf16 values as their raw
-bit patterns in a ``uint16`` array (see :func:`bf16_bits`).  Outputs are float64.
+Inputs are numpy arrays: fp32 values as ``float32``, fp16 values as
+``float16``, bf16 values as their raw bit patterns in a ``uint16`` array (see
+:func:`bf16_bits`).  Outputs are float64.
 """
 import ctypes
 import os
@@ -16,7 +17,9 @@ import numpy as np
 
 from . import build as _build
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
+MEAN, SUM, NONE = 0, 1, 2
+REDUCTIONS = {"mean": MEAN, "sum": SUM, "none": NONE}
 
 
 def default_threads() -> int:
@@ -37,9 +40,9 @@ def host_array(t) -> np.ndarray:
     import torch
     if t.dtype == torch.bfloat16:
         return bf16_bits(t)
-    if t.dtype == torch.float32:
+    if t.dtype in (torch.float32, torch.float16):
         return t.numpy()
-    raise TypeError(f"oracle inputs are fp32 or bf16, not {t.dtype}")
+    raise TypeError(f"oracle inputs are fp32, fp16 or bf16, not {t.dtype}")
 
 
 def _dtype_code(a: np.ndarray) -> int:
@@ -47,7 +50,9 @@ def _dtype_code(a: np.ndarray) -> int:
         return F32
     if a.dtype == np.uint16:
         return BF16
-    raise TypeError(f"oracle takes float32 or bf16-bits (uint16) arrays, not {a.dtype}")
+    if a.dtype == np.float16:
+        return F16
+    raise TypeError(f"oracle takes float32, float16 or bf16-bits (uint16) arrays, not {a.dtype}")
 
 
 def _row_stride(a: np.ndarray) -> int:
@@ -70,8 +75,12 @@ class Oracle:
         i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         lib.oracle_ce_count.argtypes = [p, i64, i64, i64, p, p]
         lib.oracle_ce_rows.argtypes = [p, ci, i64, p, i64, i64, i64, p, i64, p, p, ci]
+        lib.oracle_ce_rows_ex.argtypes = [p, ci, i64, p, i64, i64, i64, ci, p, p, i64, p, p, ci]
         lib.oracle_ce_mean.argtypes = [p, i64, i64]
         lib.oracle_ce_mean.restype = ctypes.c_double
+        lib.oracle_ce_sum.argtypes = [p, i64]
+        lib.oracle_ce_sum.restype = ctypes.c_double
+        lib.oracle_widen.argtypes = [p, ci, i64, p]
         lib.oracle_softmax_fwd_rows.argtypes = [p, ci, i64, i64, p, i64, p, ci]
         lib.oracle_softmax_bwd_rows.argtypes = [p, i64, p, i64, ci, i64, p, i64, p, ci]
         self.lib = lib
@@ -105,6 +114,42 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_ce_rows rejected its arguments")
         return grad, row_loss
+
+    def ce_rows_ex(self, logits: np.ndarray, targets, V: int, n: int, ignore_index: int = -100,
+                   reduction: str = "mean", grad_scale=None, rows=None, want_grad: bool = True,
+                   nthreads: int = None):
+        """ce_rows with a reduction ('mean', 'sum', 'none') and the incoming
+        grad_output: None (1), a scalar, or one value per input row for 'none'."""
+        code = _dtype_code(logits)
+        stride = _row_stride(logits)
+        t = np.ascontiguousarray(targets, dtype=np.int64)
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows = logits.shape[0] if rows is None else rows.shape[0]
+        gs = None
+        if grad_scale is not None:
+            gs = np.ascontiguousarray(np.atleast_1d(grad_scale), dtype=np.float64)
+            if reduction == "none":
+                assert gs.shape[0] == logits.shape[0]
+        grad = np.empty((nrows, V), dtype=np.float64) if want_grad else None
+        row_loss = np.empty((nrows,), dtype=np.float64)
+        rc = self.lib.oracle_ce_rows_ex(_ptr(logits), code, stride, _ptr(t), V, ignore_index, n,
+                                        REDUCTIONS[reduction], _ptr(gs), _ptr(rows), nrows,
+                                        _ptr(grad), _ptr(row_loss), nthreads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle_ce_rows_ex rejected its arguments")
+        return grad, row_loss
+
+    def ce_sum(self, row_loss) -> float:
+        rl = np.ascontiguousarray(row_loss, dtype=np.float64)
+        return self.lib.oracle_ce_sum(_ptr(rl), rl.shape[0])
+
+    def widen(self, a: np.ndarray) -> np.ndarray:
+        """The exact double value of every stored element (fp32, fp16 or bf16 bits)."""
+        a = np.ascontiguousarray(a)
+        out = np.empty(a.size, dtype=np.float64)
+        self.lib.oracle_widen(_ptr(a), _dtype_code(a), a.size, _ptr(out))
+        return out.reshape(a.shape)
 
     def ce_mean(self, row_loss, n: int) -> float:
         rl = np.ascontiguousarray(row_loss, dtype=np.float64)
@@ -180,6 +225,18 @@ def ce(*a, **k):
 
 def softmax_fwd(*a, **k):
     return get().softmax_fwd(*a, **k)
+
+
+def ce_rows_ex(*a, **k):
+    return get().ce_rows_ex(*a, **k)
+
+
+def ce_sum(*a, **k):
+    return get().ce_sum(*a, **k)
+
+
+def widen(*a, **k):
+    return get().widen(*a, **k)
 
 
 def softmax_bwd(*a, **k):

@@ -33,6 +33,13 @@
  *     softmax_kernel: y = exp(x - max x) / sum exp(x - max x) per row.
  *   - same page, _backward (block-sparse softmax backward), dense math with
  *     scale 1: dx = y * (dy - sum(y * dy)).
+ *   - Liger-Kernel, LigerCrossEntropyFunction.backward and element_mul: the
+ *     stored gradient is multiplied by the incoming grad_output when that is
+ *     not 1.
+ *   - PyTorch's CrossEntropyLoss, which the kernel docstring defers to, also
+ *     defines reduction = 'sum' (L = sum of the row losses, gradient rows not
+ *     divided by n) and 'none' (the row losses themselves; the gradient of
+ *     sum_r w_r l_r for per-row weights w_r).
  *
  * Readings where the pages are silent:
  *   - n == 0 (every row ignored): the mean is 0/0 = NaN and every gradient row
@@ -40,7 +47,10 @@
  *   - a target outside [0, V) that is not ignore_index: the row's loss is NaN,
  *     its gradient row is the unmodified input, and the row is counted as bad.
  *     Such a row still counts toward n (n counts targets != ignore_index).
- *   - bf16 inputs are widened exactly to double before any arithmetic.
+ *   - bf16 and fp16 inputs are widened exactly to double before any arithmetic.
+ *   - the gradient of a call is (p - onehot) * k_r with k_r = s / n (mean),
+ *     s (sum) or s_r (none), where s (or s_r) is the incoming grad_output
+ *     (1 when none is given).
  */
 #include <math.h>
 #include <pthread.h>
@@ -48,7 +58,26 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+enum { ORACLE_MEAN = 0, ORACLE_SUM = 1, ORACLE_NONE = 2 };
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits;
+ * exponent 0 holds zero and the subnormals (fraction * 2^-24), exponent 31
+ * holds infinities (fraction 0) and NaNs. */
+static double half_to_double(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int exp = (h >> 10) & 0x1f;
+    const int frac = h & 0x3ff;
+    double v;
+    if (exp == 0)
+        v = ldexp((double)frac, -24);
+    else if (exp == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(frac + 1024), exp - 25);
+    return sign ? -v : v;
+}
 
 /* Read element idx of a row stored as fp32 or as raw bf16 bits, widened
  * exactly to double. */
@@ -56,6 +85,8 @@ static double load_elem(const void *base, int dtype, int64_t idx)
 {
     if (dtype == ORACLE_F32)
         return (double)((const float *)base)[idx];
+    if (dtype == ORACLE_F16)
+        return half_to_double(((const uint16_t *)base)[idx]);
     uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
     float f;
     memcpy(&f, &bits, sizeof f);
@@ -66,6 +97,14 @@ static double load_elem(const void *base, int dtype, int64_t idx)
 typedef struct {
     double s, c;
 } csum_t;
+
+/* Exposed for the tests: the exact widening of n stored values to double. */
+int oracle_widen(const void *src, int dtype, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = load_elem(src, dtype, i);
+    return 0;
+}
 
 static void csum_add(csum_t *a, double v)
 {
@@ -98,9 +137,10 @@ int oracle_ce_count(const int64_t *targets, int64_t M, int64_t V, int64_t ignore
     return 0;
 }
 
-/* One cross-entropy row.  x: the row's first element; grad: V doubles or NULL. */
+/* One cross-entropy row.  x: the row's first element; grad: V doubles or NULL;
+ * k: the factor of this row's gradient ((p - onehot) * k). */
 static void ce_row(const void *x, int dtype, int64_t V, int64_t y, int64_t ignore_index,
-                   int64_t n, double *grad, double *loss)
+                   double k, double *grad, double *loss)
 {
     if (y == ignore_index) {
         if (grad)
@@ -135,7 +175,7 @@ static void ce_row(const void *x, int dtype, int64_t V, int64_t y, int64_t ignor
         for (int64_t i = 0; i < V; ++i) {
             double p = exp(load_elem(x, dtype, i) - m) / Z;
             double onehot = (i == y) ? 1.0 : 0.0;
-            grad[i] = (p - onehot) / (double)n;
+            grad[i] = (p - onehot) * k;
         }
     }
 }
@@ -178,6 +218,8 @@ typedef struct {
     int64_t b_stride;
     const int64_t *targets;
     int64_t ncols, ignore_index, n;
+    int reduction;
+    const double *grad_scale; /* NULL: 1; else one value, or one per row (none) */
     const int64_t *rows; /* NULL: rows 0..nrows-1 */
     int64_t nrows;
     double *out;       /* nrows x ncols, or NULL (cross-entropy only) */
@@ -186,6 +228,11 @@ typedef struct {
 } job_t;
 
 static size_t elem_size(int dtype) { return dtype == ORACLE_F32 ? 4 : 2; }
+
+static int valid_dtype(int dtype)
+{
+    return dtype == ORACLE_F32 || dtype == ORACLE_BF16 || dtype == ORACLE_F16;
+}
 
 static void *run_job(void *arg)
 {
@@ -196,7 +243,11 @@ static void *run_job(void *arg)
         const char *ra = (const char *)j->a + (size_t)r * (size_t)j->a_stride * es;
         double *o = j->out ? j->out + (size_t)k * (size_t)j->ncols : NULL;
         if (j->kind == JOB_CE) {
-            ce_row(ra, j->dtype, j->ncols, j->targets[r], j->ignore_index, j->n, o,
+            double s = 1.0;
+            if (j->grad_scale)
+                s = j->reduction == ORACLE_NONE ? j->grad_scale[r] : j->grad_scale[0];
+            const double kf = j->reduction == ORACLE_MEAN ? s / (double)j->n : s;
+            ce_row(ra, j->dtype, j->ncols, j->targets[r], j->ignore_index, kf, o,
                    &j->row_loss[k]);
         } else if (j->kind == JOB_SM_FWD) {
             softmax_fwd_row(ra, j->dtype, j->ncols, o);
@@ -244,14 +295,19 @@ static int run_parallel(const job_t *proto, int nthreads)
 
 /* Cross-entropy rows.  rows[k] (or k when rows is NULL) names the input row;
  * grad (nrows x V doubles, or NULL) and row_loss (nrows doubles) are indexed by
- * k.  n is the batch-wide non-ignored count from oracle_ce_count. */
-int oracle_ce_rows(const void *logits, int dtype, int64_t stride, const int64_t *targets,
-                   int64_t V, int64_t ignore_index, int64_t n, const int64_t *rows,
-                   int64_t nrows, double *grad, double *row_loss, int nthreads)
+ * k.  n is the batch-wide non-ignored count from oracle_ce_count; reduction
+ * and grad_scale (NULL, one value, or M values for ORACLE_NONE, indexed by the
+ * input row) set the gradient factor. */
+int oracle_ce_rows_ex(const void *logits, int dtype, int64_t stride, const int64_t *targets,
+                      int64_t V, int64_t ignore_index, int64_t n, int reduction,
+                      const double *grad_scale, const int64_t *rows, int64_t nrows, double *grad,
+                      double *row_loss, int nthreads)
 {
+    if (reduction != ORACLE_MEAN && reduction != ORACLE_SUM && reduction != ORACLE_NONE)
+        return 1;
     if (!logits || !targets || !row_loss || V < 1 || stride < V || nrows < 0)
         return 1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+    if (!valid_dtype(dtype))
         return 1;
     job_t j;
     memset(&j, 0, sizeof j);
@@ -263,11 +319,22 @@ int oracle_ce_rows(const void *logits, int dtype, int64_t stride, const int64_t 
     j.ncols = V;
     j.ignore_index = ignore_index;
     j.n = n;
+    j.reduction = reduction;
+    j.grad_scale = grad_scale;
     j.rows = rows;
     j.nrows = nrows;
     j.out = grad;
     j.row_loss = row_loss;
     return run_parallel(&j, nthreads);
+}
+
+/* The mean-reduced call without a grad_output (the fused forward+backward). */
+int oracle_ce_rows(const void *logits, int dtype, int64_t stride, const int64_t *targets,
+                   int64_t V, int64_t ignore_index, int64_t n, const int64_t *rows,
+                   int64_t nrows, double *grad, double *row_loss, int nthreads)
+{
+    return oracle_ce_rows_ex(logits, dtype, stride, targets, V, ignore_index, n, ORACLE_MEAN, NULL,
+                             rows, nrows, grad, row_loss, nthreads);
 }
 
 /* L = sum_r row_loss[r] / n over all M rows (ignored rows hold 0). */
@@ -279,12 +346,21 @@ double oracle_ce_mean(const double *row_loss, int64_t M, int64_t n)
     return csum_value(&s) / (double)n;
 }
 
+/* L = sum_r row_loss[r] over all M rows (reduction = 'sum'). */
+double oracle_ce_sum(const double *row_loss, int64_t M)
+{
+    csum_t s = {0.0, 0.0};
+    for (int64_t r = 0; r < M; ++r)
+        csum_add(&s, row_loss[r]);
+    return csum_value(&s);
+}
+
 int oracle_softmax_fwd_rows(const void *x, int dtype, int64_t stride, int64_t N,
                             const int64_t *rows, int64_t nrows, double *y, int nthreads)
 {
     if (!x || !y || N < 1 || stride < N || nrows < 0)
         return 1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+    if (!valid_dtype(dtype))
         return 1;
     job_t j;
     memset(&j, 0, sizeof j);
@@ -305,7 +381,7 @@ int oracle_softmax_bwd_rows(const void *y, int64_t y_stride, const void *dy, int
 {
     if (!y || !dy || !dx || N < 1 || y_stride < N || dy_stride < N || nrows < 0)
         return 1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+    if (!valid_dtype(dtype))
         return 1;
     job_t j;
     memset(&j, 0, sizeof j);

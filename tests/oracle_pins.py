@@ -350,9 +350,80 @@ def pin_finite_difference_softmax_bwd(o):
         assert abs(fd - dx[j]) < 1e-6, f"softmax backward finite difference at {j}"
 
 
+# ---------------------------------------------------------------------------
+# reductions, the incoming grad_output, fp16 inputs
+
+def pin_decoding_exhaustive(o):
+    """Every fp16 and every bf16 bit pattern widens to the value numpy / torch give."""
+    h = np.arange(65536, dtype=np.uint16).view(np.float16)
+    assert np.array_equal(o.widen(h), h.astype(np.float64), equal_nan=True), "fp16 decoding"
+    b = np.arange(65536, dtype=np.uint16)
+    ref = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(o.widen(b), ref, equal_nan=True), "bf16 decoding"
+
+
+def _as_host(t):
+    if t.dtype == torch.bfloat16:
+        return workloads_bits(t)
+    return t.numpy()
+
+
+def pin_torch_reductions(o):
+    """F.cross_entropy with reduction sum / none / mean and a grad_output, float64 autograd."""
+    rng = np.random.default_rng(21)
+    for dtype in (torch.float32, torch.bfloat16, torch.float16):
+        M, V = 9, 37
+        x = (torch.from_numpy(rng.standard_normal((M, V))) * 2).to(dtype)
+        t = torch.from_numpy(rng.integers(0, V, M))
+        t[[1, 6]] = II
+        x64 = x.to(torch.float64)
+        n, _ = o.ce_count(t.numpy(), V, II)
+        w = torch.from_numpy(rng.standard_normal(M))
+        for reduction, go in (("mean", torch.tensor(2.5, dtype=torch.float64)),
+                              ("sum", torch.tensor(-0.75, dtype=torch.float64)),
+                              ("none", w)):
+            xr = x64.clone().requires_grad_(True)
+            out = F.cross_entropy(xr, t, ignore_index=II, reduction=reduction)
+            out.backward(go)
+            scale = go.numpy() if reduction == "none" else float(go)
+            grad, rl = o.ce_rows_ex(_as_host(x), t.numpy(), V, n, II, reduction, scale)
+            _close(grad, xr.grad.numpy(), 1e-10, 1e-18, f"torch {reduction} gradient {dtype}")
+            if reduction == "none":
+                _close(rl, out.detach().numpy(), 1e-12, 1e-15, f"torch none losses {dtype}")
+            elif reduction == "sum":
+                _close(o.ce_sum(rl), out.item(), 1e-12, 0, f"torch sum loss {dtype}")
+            else:
+                _close(o.ce_mean(rl, n), out.item(), 1e-12, 0, f"torch mean loss {dtype}")
+
+
+def pin_reduction_invariants(o):
+    rng = np.random.default_rng(22)
+    M, V = 10, 29
+    x = _dyadic_logits(rng, M, V)
+    t = rng.integers(0, V, M)
+    t[4] = II
+    n, _ = o.ce_count(t, V, II)
+    g_mean, l_mean = o.ce_rows_ex(x, t, V, n, II, "mean")
+    g_sum, l_sum = o.ce_rows_ex(x, t, V, n, II, "sum")
+    g_none, _ = o.ce_rows_ex(x, t, V, n, II, "none", np.ones(M))
+    _close(g_sum, g_mean * n, 1e-13, 1e-18, "sum gradient is n times the mean gradient")
+    _close(g_none, g_sum, 0, 0, "none with unit weights is the sum gradient")
+    assert np.array_equal(l_mean, l_sum), "row losses do not depend on the reduction"
+    g_s, _ = o.ce_rows_ex(x, t, V, n, II, "mean", 2.5)
+    _close(g_s, 2.5 * g_mean, 1e-13, 1e-18, "the gradient is linear in grad_output")
+    wts = rng.standard_normal(M)
+    g_w, _ = o.ce_rows_ex(x, t, V, n, II, "none", wts)
+    _close(g_w, wts[:, None] * g_sum, 1e-12, 1e-18, "per-row weights scale their rows")
+    sel = np.array([7, 2, 9])
+    g_sel, l_sel = o.ce_rows_ex(x, t, V, n, II, "none", wts, rows=sel)
+    _close(g_sel, g_w[sel], 0, 0, "a row subset picks the rows' own weights")
+    assert np.array_equal(l_sel, l_sum[sel])
+
+
 ALL_PINS = [
     pin_golden_ce, pin_golden_softmax, pin_uniform_closed_form, pin_softmax_uniform,
     pin_ce_invariants, pin_neginf_columns, pin_v1_and_degenerate, pin_softmax_invariants,
     pin_bf16_decoding, pin_row_stride, pin_torch_cross_entropy, pin_torch_softmax,
     pin_finite_difference_ce, pin_finite_difference_softmax_bwd,
+    pin_decoding_exhaustive, pin_torch_reductions, pin_reduction_invariants,
 ]

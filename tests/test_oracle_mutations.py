@@ -14,8 +14,18 @@ MUTANTS = [
     ("drop_onehot", "double onehot = (i == y) ? 1.0 : 0.0;", "double onehot = 0.0;"),
     ("onehot_wrong_column", "double onehot = (i == y) ? 1.0 : 0.0;",
      "double onehot = (i == (y + 1) % V) ? 1.0 : 0.0;"),
-    ("divide_by_n_plus_1", "grad[i] = (p - onehot) / (double)n;",
-     "grad[i] = (p - onehot) / (double)(n + 1);"),
+    ("divide_by_n_plus_1", "const double kf = j->reduction == ORACLE_MEAN ? s / (double)j->n : s;",
+     "const double kf = j->reduction == ORACLE_MEAN ? s / (double)(j->n + 1) : s;"),
+    ("sum_divides_by_n", "const double kf = j->reduction == ORACLE_MEAN ? s / (double)j->n : s;",
+     "const double kf = j->reduction != ORACLE_NONE ? s / (double)j->n : s;"),
+    ("grad_scale_ignored", "            if (j->grad_scale)\n",
+     "            if (0)\n"),
+    ("none_scale_wrong_row", "s = j->reduction == ORACLE_NONE ? j->grad_scale[r] : j->grad_scale[0];",
+     "s = j->reduction == ORACLE_NONE ? j->grad_scale[k] : j->grad_scale[0];"),
+    ("half_exponent_bias", "v = ldexp((double)(frac + 1024), exp - 25);",
+     "v = ldexp((double)(frac + 1024), exp - 24);"),
+    ("half_subnormal_scale", "v = ldexp((double)frac, -24);",
+     "v = ldexp((double)frac, -25);"),
     ("loss_sign", "*loss = m + log(Z) - load_elem(x, dtype, y);",
      "*loss = m - log(Z) - load_elem(x, dtype, y);"),
     ("loss_drops_max", "*loss = m + log(Z) - load_elem(x, dtype, y);",
