@@ -14,11 +14,12 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libgbce.so")
 
-GBCE_F32, GBCE_BF16 = 0, 1
-DTYPES = {torch.float32: GBCE_F32, torch.bfloat16: GBCE_BF16}
+GBCE_F32, GBCE_BF16, GBCE_F16 = 0, 1, 2
+DTYPES = {torch.float32: GBCE_F32, torch.bfloat16: GBCE_BF16, torch.float16: GBCE_F16}
+REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 OK, ERR_NULL, ERR_SIZE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA, ERR_BAD_TARGET, ERR_TIMEOUT, \
-    ERR_NO_DEVICE = range(9)
+    ERR_NO_DEVICE, ERR_REDUCTION = range(10)
 
 _lib = None
 
@@ -41,6 +42,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ce_fwd_bwd.argtypes = [p, i64, p, p, i64, i64, i64, ci, p]
         lib.softmax_fwd.argtypes = [p, i64, p, i64, i64, i64, ci, p]
         lib.softmax_bwd.argtypes = [p, i64, p, i64, p, i64, i64, i64, ci, p]
+        lib.ce_fwd_bwd_ex.argtypes = [p, i64, p, p, p, p, i64, i64, i64, ci, ci, p]
+        lib.scale_rows.argtypes = [p, i64, i64, i64, ci, p, ci, p]
         lib.gbce_last_error.argtypes = [p]
         lib.gbce_status_string.argtypes = [ci]
         lib.gbce_status_string.restype = ctypes.c_char_p
@@ -48,7 +51,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gbce_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
                                          ctypes.POINTER(ctypes.c_int64)]
         for f in ("ce_fwd_bwd", "softmax_fwd", "softmax_bwd", "gbce_last_error",
-                  "gbce_timing_enable", "gbce_timing_read"):
+                  "gbce_timing_enable", "gbce_timing_read", "ce_fwd_bwd_ex", "scale_rows"):
             getattr(lib, f).restype = ci
         _lib = lib
     return _lib
@@ -70,7 +73,7 @@ def _matrix(t: torch.Tensor, name: str):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype not in DTYPES:
-        raise TypeError(f"{name} must be float32 or bfloat16, not {t.dtype}")
+        raise TypeError(f"{name} must be float32, bfloat16 or float16, not {t.dtype}")
     if t.shape[1] > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} needs unit column stride")
     stride = t.stride(0) if t.shape[0] > 1 else t.shape[1]
@@ -103,6 +106,108 @@ def ce_fwd_bwd(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = 
                                    _stream_handle(stream))
     _check(rc, "ce_fwd_bwd")
     return loss
+
+
+def _device_floats(v, n: int, device, name: str):
+    """A float32 CUDA tensor of n values on `device` from a tensor or a number."""
+    if not torch.is_tensor(v):
+        v = torch.full((n,), float(v), dtype=torch.float32, device=device)
+    if v.dtype != torch.float32 or not v.is_cuda or v.numel() != n or not v.is_contiguous():
+        raise ValueError(f"{name} must be {n} contiguous float32 CUDA value(s)")
+    return v
+
+
+def ce_fwd_bwd_ex(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+                  reduction: str = "mean", grad_scale=None, want_row_loss: bool = False,
+                  loss: torch.Tensor = None, row_loss: torch.Tensor = None, stream=None):
+    """Cross-entropy with a reduction ('mean', 'sum', 'none'), optional per-row
+    losses, and grad_scale (None, a number or a float32 CUDA tensor: one value,
+    or one per row for 'none') folded into the in-place gradient.
+
+    Returns (loss, row_loss): loss is a 0-dim float32 CUDA tensor (None for
+    'none'); row_loss is [M] float32 when requested or for 'none', else None.
+    """
+    lp, stride, M, V = _matrix(logits, "logits")
+    if reduction not in REDUCTIONS:
+        raise ValueError(f"reduction must be one of {sorted(REDUCTIONS)}")
+    if targets.dtype != torch.int64 or targets.dim() != 1 or targets.shape[0] != M:
+        raise ValueError("targets must be int64 of shape [M]")
+    if M and (not targets.is_cuda or not targets.is_contiguous()):
+        raise ValueError("targets must be a contiguous CUDA tensor")
+    dev = logits.device
+    if reduction != "none" and loss is None:
+        loss = torch.empty((), dtype=torch.float32, device=dev)
+    if (want_row_loss or reduction == "none") and row_loss is None:
+        row_loss = torch.empty((M,), dtype=torch.float32, device=dev)
+    gs = None
+    if grad_scale is not None:
+        gs = _device_floats(grad_scale, M if reduction == "none" else 1, dev, "grad_scale")
+    rc = load_library().ce_fwd_bwd_ex(
+        lp, stride, targets.data_ptr(), None if loss is None else loss.data_ptr(),
+        None if row_loss is None else row_loss.data_ptr(), None if gs is None else gs.data_ptr(),
+        M, V, int(ignore_index), DTYPES[logits.dtype], REDUCTIONS[reduction],
+        _stream_handle(stream))
+    _check(rc, "ce_fwd_bwd_ex")
+    return (None if reduction == "none" else loss), row_loss
+
+
+def scale_rows(x: torch.Tensor, scale, stream=None) -> torch.Tensor:
+    """x *= scale in place; scale is a number, a one-element float32 CUDA tensor,
+    or one value per row ([M]).  A single scale of 1 costs only the launch."""
+    xp, stride, M, N = _matrix(x, "x")
+    per_row = torch.is_tensor(scale) and scale.numel() == M and M != 1
+    sc = _device_floats(scale, M if per_row else 1, x.device, "scale")
+    rc = load_library().scale_rows(xp, stride, M, N, DTYPES[x.dtype], sc.data_ptr(),
+                                   1 if per_row else 0, _stream_handle(stream))
+    _check(rc, "scale_rows")
+    return x
+
+
+class FusedCrossEntropy(torch.autograd.Function):
+    """Autograd form of the fused call (the behaviour of Liger-Kernel's
+    LigerCrossEntropyFunction): the forward computes the loss and writes the
+    gradient into the logits' storage, which it saves; the backward scales that
+    gradient in place by grad_output (a device-side no-op when it is 1, so no
+    host synchronisation) and returns it.  The logits' values are consumed:
+    read them before this call, and call backward once.
+    """
+
+    @staticmethod
+    def forward(ctx, logits, targets, ignore_index=-100, reduction="mean"):
+        buf = logits.detach()
+        loss, row_loss = ce_fwd_bwd_ex(buf, targets, ignore_index, reduction)
+        ctx.save_for_backward(buf)
+        ctx.reduction = reduction
+        return row_loss if reduction == "none" else loss
+
+    @staticmethod
+    def backward(ctx, grad_output):
+        (grad,) = ctx.saved_tensors
+        scale_rows(grad, grad_output.detach().to(torch.float32).contiguous().reshape(-1))
+        return grad, None, None, None
+
+
+def cross_entropy(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
+                  reduction: str = "mean", inplace: bool = True) -> torch.Tensor:
+    """Hard-label cross-entropy of [M, V] logits, differentiable.  With
+    inplace=True the logits' storage is reused for the gradient (no extra
+    M x V buffer); with inplace=False the logits are copied first."""
+    if not inplace:
+        logits = logits.clone(memory_format=torch.contiguous_format)
+    return FusedCrossEntropy.apply(logits, targets, ignore_index, reduction)
+
+
+class CrossEntropyLoss(torch.nn.Module):
+    """nn.Module form of cross_entropy (hard labels, ignore_index, reduction)."""
+
+    def __init__(self, ignore_index: int = -100, reduction: str = "mean", inplace: bool = True):
+        super().__init__()
+        if reduction not in REDUCTIONS:
+            raise ValueError(f"reduction must be one of {sorted(REDUCTIONS)}")
+        self.ignore_index, self.reduction, self.inplace = ignore_index, reduction, inplace
+
+    def forward(self, logits, targets):
+        return cross_entropy(logits, targets, self.ignore_index, self.reduction, self.inplace)
 
 
 def softmax_fwd(x: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.Tensor:

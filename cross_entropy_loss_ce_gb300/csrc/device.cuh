@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace gbce {
 
@@ -160,7 +161,7 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 }
 
 // ---------------------------------------------------------------------------
-// element types: 16-byte vectors of fp32 (4) or bf16 (8)
+// element types: 16-byte vectors of fp32 (4), bf16 (8) or fp16 (8)
 
 template <typename T>
 struct Elem;
@@ -168,6 +169,7 @@ struct Elem;
 template <>
 struct Elem<float> {
     static constexpr int kPerVec = 4;
+    static constexpr uint32_t kNegInfPair = 0xff800000u;  // -inf (never read as pairs)
     __device__ static __forceinline__ void unpack(const uint4 &v, float (&f)[4])
     {
         f[0] = __uint_as_float(v.x);
@@ -187,6 +189,18 @@ struct Elem<float> {
 template <>
 struct Elem<__nv_bfloat16> {
     static constexpr int kPerVec = 8;
+    static constexpr uint32_t kNegInfPair = 0xff80ff80u;  // two bf16 -inf
+    // element-wise max of two packed pairs, and the larger of a pair as fp32
+    __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b)
+    {
+        __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                   *reinterpret_cast<const __nv_bfloat162 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+    __device__ static __forceinline__ float pair_max(uint32_t p)
+    {
+        return fmaxf(__uint_as_float(p << 16), __uint_as_float(p & 0xffff0000u));
+    }
     __device__ static __forceinline__ void unpack(const uint4 &v, float (&f)[8])
     {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -214,6 +228,45 @@ struct Elem<__nv_bfloat16> {
     {
         *p = __float2bfloat16_rn(v);
     }
+};
+
+template <>
+struct Elem<__half> {
+    static constexpr int kPerVec = 8;
+    static constexpr uint32_t kNegInfPair = 0xfc00fc00u;  // two fp16 -inf
+    __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b)
+    {
+        __half2 r = __hmax2(*reinterpret_cast<const __half2 *>(&a),
+                            *reinterpret_cast<const __half2 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+    __device__ static __forceinline__ float pair_max(uint32_t p)
+    {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&p));
+        return fmaxf(f.x, f.y);
+    }
+    __device__ static __forceinline__ void unpack(const uint4 &v, float (&f)[8])
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    __device__ static __forceinline__ uint32_t pack2(float lo, float hi)
+    {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ static __forceinline__ uint4 pack(const float (&f)[8])
+    {
+        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
+                          pack2(f[6], f[7]));
+    }
+    __device__ static __forceinline__ float load(const __half *p) { return __half2float(*p); }
+    __device__ static __forceinline__ void store(__half *p, float v) { *p = __float2half_rn(v); }
 };
 
 // ---------------------------------------------------------------------------

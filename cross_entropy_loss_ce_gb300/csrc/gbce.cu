@@ -151,7 +151,11 @@ KernelFn pick_kernel(const Plan &p)
 template <Op OP>
 KernelFn pick(int dtype, const Plan &p)
 {
-    return dtype == GBCE_F32 ? pick_kernel<OP, float>(p) : pick_kernel<OP, __nv_bfloat16>(p);
+    switch (dtype) {
+    case GBCE_F32: return pick_kernel<OP, float>(p);
+    case GBCE_F16: return pick_kernel<OP, __half>(p);
+    default: return pick_kernel<OP, __nv_bfloat16>(p);
+    }
 }
 
 // Per-device one-time function attributes (large dynamic shared memory,
@@ -378,7 +382,7 @@ int check_matrix(const void *p, int64_t stride, int64_t M, int64_t cols, int dty
 
 int check_common(int64_t M, int64_t cols, int dtype)
 {
-    if (dtype != GBCE_F32 && dtype != GBCE_BF16)
+    if (dtype != GBCE_F32 && dtype != GBCE_BF16 && dtype != GBCE_F16)
         return GBCE_ERR_DTYPE;
     if (M < 0 || cols < 1 || cols > INT32_MAX || M > kMaxRows)
         return GBCE_ERR_SIZE;
@@ -399,16 +403,21 @@ bool same_phase(const void *a, int64_t sa, const void *b, int64_t sb, size_t esi
 // n, [kCeScratchHeader, + 4 M) the row losses.
 constexpr size_t kCeScratchHeader = 256;
 
-// The cross-entropy launches on `stream`: the count kernel (n; the NaN mean
-// when M == 0), the row kernel, then the mean kernel, each of the last two
-// launched as a programmatic dependent of the one before.
-cudaError_t launch_ce(void *logits, int64_t stride, const int64_t *targets, float *loss, int64_t M,
-                      int64_t V, int64_t ignore_index, int dtype, void *scratch,
+// The cross-entropy launches on `stream`: the count kernel (n; the reduced
+// loss itself when M == 0), the row kernel, then (mean, sum) the mean kernel,
+// each of the last two a programmatic dependent of the one before.  scratch
+// holds n at [0, 4); row losses go to `row_loss` when given, else to scratch
+// at [kCeScratchHeader, + 4 M).
+cudaError_t launch_ce(void *logits, int64_t stride, const int64_t *targets, float *loss,
+                      float *row_loss, const float *grad_scale, int64_t M, int64_t V,
+                      int64_t ignore_index, int dtype, int reduction, void *scratch,
                       cudaStream_t stream)
 {
     int *n_ptr = static_cast<int *>(scratch);
-    float *row_loss = reinterpret_cast<float *>(static_cast<char *>(scratch) + kCeScratchHeader);
-    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr, loss);
+    if (!row_loss)
+        row_loss = reinterpret_cast<float *>(static_cast<char *>(scratch) + kCeScratchHeader);
+    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr, loss,
+                                                   reduction);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || M == 0)
         return e;
@@ -424,12 +433,14 @@ cudaError_t launch_ce(void *logits, int64_t stride, const int64_t *targets, floa
     a.ignore_index = ignore_index;
     a.n_ptr = n_ptr;
     a.row_loss = row_loss;
+    a.reduction = reduction;
+    a.grad_scale = grad_scale;
     a.C = p.C;
     a.per_vec = p.per_vec;
     a.chunk_vec = p.chunk_vec;
     a.nslot = p.nslot;
     e = launch_rows(pick<Op::CE>(dtype, p), p, a, stream, true);
-    if (e != cudaSuccess)
+    if (e != cudaSuccess || reduction == GBCE_NONE)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
@@ -441,7 +452,32 @@ cudaError_t launch_ce(void *logits, int64_t stride, const int64_t *targets, floa
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, ce_mean_kernel<1024>, static_cast<const float *>(row_loss), M,
-                              static_cast<const int *>(n_ptr), loss);
+                              static_cast<const int *>(n_ptr), loss, reduction);
+}
+
+// ce_fwd_bwd_ex with its temporary storage from the pool.
+int ce_call(void *logits, int64_t stride, const int64_t *targets, float *loss, float *row_loss,
+            const float *grad_scale, int64_t M, int64_t V, int64_t ignore_index, int dtype,
+            int reduction, cudaStream_t stream)
+{
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return map_error(e);
+    cudaMemPool_t pool;
+    if ((e = pool_for(device, &pool)) != cudaSuccess)
+        return map_error(e);
+    void *scratch = nullptr;
+    const size_t bytes =
+        kCeScratchHeader + (row_loss ? 0 : static_cast<size_t>(M) * sizeof(float));
+    if ((e = cudaMallocFromPoolAsync(&scratch, bytes, pool, stream)) != cudaSuccess)
+        return map_error(e);
+    e = launch_ce(logits, stride, targets, loss, row_loss, grad_scale, M, V, ignore_index, dtype,
+                  reduction, scratch, stream);
+    cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e == cudaSuccess)
+        e = ef;
+    return map_error(e);
 }
 
 }  // namespace
@@ -462,24 +498,63 @@ extern "C" int ce_fwd_bwd(void *logits, int64_t stride, const int64_t *targets, 
         return st;
     if (!aligned_to(targets, 8) || !aligned_to(loss, 4))
         return GBCE_ERR_ALIGN;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    return ce_call(logits, stride, targets, loss, nullptr, nullptr, M, V, ignore_index, dtype,
+                   GBCE_MEAN, reinterpret_cast<cudaStream_t>(stream_));
+}
 
-    int device = 0;
-    cudaError_t e = cudaGetDevice(&device);
-    if (e != cudaSuccess)
-        return map_error(e);
-    cudaMemPool_t pool;
-    if ((e = pool_for(device, &pool)) != cudaSuccess)
-        return map_error(e);
-    void *scratch = nullptr;
-    const size_t bytes = kCeScratchHeader + static_cast<size_t>(M) * sizeof(float);
-    if ((e = cudaMallocFromPoolAsync(&scratch, bytes, pool, stream)) != cudaSuccess)
-        return map_error(e);
-    e = launch_ce(logits, stride, targets, loss, M, V, ignore_index, dtype, scratch, stream);
-    cudaError_t ef = cudaFreeAsync(scratch, stream);
-    if (e == cudaSuccess)
-        e = ef;
-    return map_error(e);
+extern "C" int ce_fwd_bwd_ex(void *logits, int64_t stride, const int64_t *targets, float *loss,
+                             float *row_loss, const float *grad_scale, int64_t M, int64_t V,
+                             int64_t ignore_index, int dtype, int reduction,
+                             gbce_stream_t stream_)
+{
+    int st = check_common(M, V, dtype);
+    if (st)
+        return st;
+    if (reduction != GBCE_MEAN && reduction != GBCE_SUM && reduction != GBCE_NONE)
+        return GBCE_ERR_REDUCTION;
+    if ((reduction != GBCE_NONE && !loss) || (reduction == GBCE_NONE && M > 0 && !row_loss) ||
+        (M > 0 && !targets))
+        return GBCE_ERR_NULL;
+    if ((st = check_matrix(logits, stride, M, V, dtype)))
+        return st;
+    if (!aligned_to(targets, 8) || !aligned_to(loss, 4) || !aligned_to(row_loss, 16) ||
+        !aligned_to(grad_scale, 4))
+        return GBCE_ERR_ALIGN;
+    return ce_call(logits, stride, targets, reduction == GBCE_NONE ? nullptr : loss, row_loss,
+                   grad_scale, M, V, ignore_index, dtype, reduction,
+                   reinterpret_cast<cudaStream_t>(stream_));
+}
+
+extern "C" int scale_rows(void *x, int64_t stride, int64_t M, int64_t N, int dtype,
+                          const float *scale, int per_row, gbce_stream_t stream_)
+{
+    int st = check_common(M, N, dtype);
+    if (st)
+        return st;
+    if (M > 0 && !scale)
+        return GBCE_ERR_NULL;
+    if ((st = check_matrix(x, stride, M, N, dtype)))
+        return st;
+    if (!aligned_to(scale, 4))
+        return GBCE_ERR_ALIGN;
+    if (M == 0)
+        return GBCE_OK;
+    const int64_t sms = current_sm_count();
+    const int64_t grid = M < sms * 8 ? M : (sms > 0 ? sms * 8 : M);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const unsigned g = static_cast<unsigned>(grid);
+    switch (dtype) {
+    case GBCE_F32:
+        scale_rows_kernel<float, 256><<<g, 256, 0, stream>>>(x, stride, M, N, scale, per_row);
+        break;
+    case GBCE_F16:
+        scale_rows_kernel<__half, 256><<<g, 256, 0, stream>>>(x, stride, M, N, scale, per_row);
+        break;
+    default:
+        scale_rows_kernel<__nv_bfloat16, 256><<<g, 256, 0, stream>>>(x, stride, M, N, scale,
+                                                                      per_row);
+    }
+    return map_error(cudaGetLastError());
 }
 
 extern "C" int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_stride, int64_t M,
@@ -574,6 +649,7 @@ extern "C" const char *gbce_status_string(int status)
     case GBCE_ERR_BAD_TARGET: return "a target is outside [0, V) and is not ignore_index";
     case GBCE_ERR_TIMEOUT: return "a bounded wait for an asynchronous copy gave up";
     case GBCE_ERR_NO_DEVICE: return "no usable CUDA device";
+    case GBCE_ERR_REDUCTION: return "reduction is not a gbce_reduction";
     default: return "unknown status";
     }
 }
@@ -683,6 +759,7 @@ extern "C" int ce_fwd_bwd_noalloc(void *logits, int64_t stride, const int64_t *t
     // ce_count_kernel overwrites the count and the row kernel writes the loss
     // of every row 0..M-1 before the mean kernel reads them: nothing left by
     // an earlier call is read.
-    e = launch_ce(logits, stride, targets, loss, M, V, ignore_index, dtype, scratch, stream);
+    e = launch_ce(logits, stride, targets, loss, nullptr, nullptr, M, V, ignore_index, dtype,
+                  GBCE_MEAN, scratch, stream);
     return map_error(e);
 }

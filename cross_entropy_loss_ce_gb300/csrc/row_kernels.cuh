@@ -28,6 +28,9 @@ constexpr int kMaxChunks = 8;  // bulk copies (one mbarrier each) per CTA slice
 
 enum class Op { CE, SoftmaxFwd, SoftmaxBwd };
 
+// Reductions of the cross-entropy (the values of gbce_reduction).
+enum : int { kReduceMean = 0, kReduceSum = 1, kReduceNone = 2 };
+
 struct RowArgs {
     const void *in0;  // logits (CE), x (softmax fwd), y (softmax bwd)
     int64_t s0;
@@ -41,6 +44,8 @@ struct RowArgs {
     int64_t ignore_index;
     const int *n_ptr;   // non-ignored row count, written by ce_count_kernel
     float *row_loss;    // [M]
+    int reduction;      // kReduceMean / kReduceSum / kReduceNone
+    const float *grad_scale;  // NULL (1), one value, or one per row (kReduceNone)
     // launch plan
     int C;          // CTAs per row (cluster size)
     int per_vec;    // 16-byte vectors per CTA slice (capacity of one staged buffer)
@@ -87,6 +92,19 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads)
 __device__ __forceinline__ void wait_prerequisite_grid()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// A cross-entropy gradient row is (p - onehot) * k with k = s / n (mean) or s
+// (sum, none), s the incoming grad_output (1 when absent, per row for none).
+// Returns scale = k / D (for exp(x - M)) and sub = k (the one-hot term); for
+// the mean without a grad_output these are 1 / (D n) and 1 / n.
+__device__ __forceinline__ void ce_row_factor(const RowArgs &a, int64_t row, float D, float n,
+                                              float &scale, float &sub)
+{
+    const float kn = a.reduction == kReduceMean ? n : 1.f;
+    const float s = a.grad_scale ? __ldg(a.grad_scale + (a.reduction == kReduceNone ? row : 0)) : 1.f;
+    scale = s / (D * kn);
+    sub = s / kn;
 }
 
 // sum_{r < M} row_loss[r] by NTH threads (tid < NTH, all calling, synchronised
@@ -208,7 +226,8 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
         const int j = lane + 32 * v;
-        r0[v] = j < cnt ? __ldcs(src0 + j) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+        r0[v] = j < cnt ? __ldcs(src0 + j)
+                        : make_uint4(E::kNegInfPair, E::kNegInfPair, E::kNegInfPair, E::kNegInfPair);
         if constexpr (NBUF == 2)
             r1[v] = j < cnt ? __ldcs(reinterpret_cast<const uint4 *>(in1 + g.head) + j)
                             : make_uint4(0u, 0u, 0u, 0u);
@@ -268,15 +287,11 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
         if (tail_here)
             m = fmaxf(m, t0);
         if constexpr (VEC == 8) {
-            __nv_bfloat162 mm = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+            uint32_t mm = E::kNegInfPair;
 #pragma unroll
-            for (int v = 0; v < VPL; ++v) {
-                const uint32_t w[4] = {r0[v].x, r0[v].y, r0[v].z, r0[v].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    mm = __hmax2(mm, *reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
-            }
-            m = fmaxf(m, fmaxf(__low2float(mm), __high2float(mm)));
+            for (int v = 0; v < VPL; ++v)
+                mm = E::max2(E::max2(mm, r0[v].x), E::max2(r0[v].y, E::max2(r0[v].z, r0[v].w)));
+            m = fmaxf(m, E::pair_max(mm));
         } else {
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
@@ -313,9 +328,7 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
         float scale, sub = 0.f;
         if constexpr (OP == Op::CE) {
             wait_prerequisite_grid();  // n comes from the count kernel
-            const float n = static_cast<float>(*a.n_ptr);
-            scale = 1.f / (d * n);
-            sub = 1.f / n;
+            ce_row_factor(a, row, d, static_cast<float>(*a.n_ptr), scale, sub);
         } else {
             scale = 1.f / d;
         }
@@ -513,16 +526,13 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
             const int c1 = (k + 1) * a.chunk_vec < cnt ? (k + 1) * a.chunk_vec : cnt;
             if (ok) {
                 if constexpr (VEC == 8) {
-                    // bf16: packed max of element pairs, no unpacking
-                    __nv_bfloat162 mm = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+                    // 16-bit types: packed max of element pairs, no unpacking
+                    uint32_t mm = E::kNegInfPair;
                     for (int j = k * a.chunk_vec + tid; j < c1; j += NT) {
                         const uint4 v = ld_shared_v4(buf0 + j * 16u);
-                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            mm = __hmax2(mm, *reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                        mm = E::max2(E::max2(mm, v.x), E::max2(v.y, E::max2(v.z, v.w)));
                     }
-                    m = fmaxf(m, fmaxf(__low2float(mm), __high2float(mm)));
+                    m = fmaxf(m, E::pair_max(mm));
                 } else {
                     for (int j = k * a.chunk_vec + tid; j < c1; j += NT) {
                         float f[VEC];
@@ -594,9 +604,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
             float scale, sub = 0.f;
             if constexpr (OP == Op::CE) {
                 wait_prerequisite_grid();  // n comes from the count kernel
-                const float n = static_cast<float>(*a.n_ptr);
-                scale = 1.f / (D * n);
-                sub = 1.f / n;
+                ce_row_factor(a, row, D, static_cast<float>(*a.n_ptr), scale, sub);
             } else {
                 scale = 1.f / D;
             }
@@ -929,23 +937,20 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
 #pragma unroll
                         for (int v = 0; v < VPT; ++v) {
                             const int j = tid + v * NC;
-                            // a vector past the slice end reads as bf16 -inf pairs (fp32 skips it)
+                            // a vector past the slice end reads as -inf pairs (fp32 code skips it)
                             raw[v] = j < cn ? ld_shared_v4(b0 + j * 16u)
-                                            : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u,
-                                                         0xff80ff80u);
+                                            : make_uint4(E::kNegInfPair, E::kNegInfPair,
+                                                         E::kNegInfPair, E::kNegInfPair);
                         }
                         // the chunk's max first (packed pairs for bf16), then one rescale and the sum
                         float cm = -INFINITY;
                         if constexpr (VEC == 8) {
-                            __nv_bfloat162 mm = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+                            uint32_t mm = E::kNegInfPair;
 #pragma unroll
-                            for (int v = 0; v < VPT; ++v) {
-                                const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    mm = __hmax2(mm, *reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
-                            }
-                            cm = fmaxf(__low2float(mm), __high2float(mm));
+                            for (int v = 0; v < VPT; ++v)
+                                mm = E::max2(E::max2(mm, raw[v].x),
+                                             E::max2(raw[v].y, E::max2(raw[v].z, raw[v].w)));
+                            cm = E::pair_max(mm);
                         } else {
 #pragma unroll
                             for (int v = 0; v < VPT; ++v) {
@@ -1039,12 +1044,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
             float scale = 0.f, sub = 0.f, ML = 0.f;
             if constexpr (OP != Op::SoftmaxBwd) {
                 ML = r.x * kLog2e;
-                if constexpr (OP == Op::CE) {
-                    scale = 1.f / (r.y * nf);
-                    sub = 1.f / nf;
-                } else {
+                if constexpr (OP == Op::CE)
+                    ce_row_factor(a, row, r.y, nf, scale, sub);
+                else
                     scale = 1.f / r.y;
-                }
             }
             const bool all_ok = r.z == 0.f;
             const int64_t ycol = y - body;
@@ -1274,9 +1277,7 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
         float scale, sub = 0.f;
         if constexpr (OP == Op::CE) {
             wait_prerequisite_grid();  // n comes from the count kernel
-            const float n = static_cast<float>(*a.n_ptr);
-            scale = 1.f / (r.y * n);
-            sub = 1.f / n;
+            ce_row_factor(a, row, r.y, static_cast<float>(*a.n_ptr), scale, sub);
         } else {
             scale = 1.f / r.y;
         }
@@ -1297,13 +1298,13 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
 
 // ---------------------------------------------------------------------------
 // n = number of targets != ignore_index (one CTA); flags targets outside [0, V);
-// for M == 0 writes the mean 0/0 = NaN itself.  It lets the row kernel launch
+// for M == 0 writes the reduced loss itself (mean 0/0 = NaN, sum 0).  It lets the row kernel launch
 // at once (programmatic dependent launch); the row kernel waits for it on the
 // device before it reads n.
 template <int NT>
 __global__ void __launch_bounds__(NT) ce_count_kernel(const int64_t *targets, int64_t M, int64_t V,
                                                       int64_t ignore_index, int *n_out,
-                                                      float *loss)
+                                                      float *loss, int reduction)
 {
     __shared__ int warp_n[NT / 32];
     __shared__ int any_bad;
@@ -1336,8 +1337,8 @@ __global__ void __launch_bounds__(NT) ce_count_kernel(const int64_t *targets, in
             n += __shfl_xor_sync(0xffffffffu, n, off);
         if (threadIdx.x == 0) {
             *n_out = n;
-            if (M == 0)
-                *loss = __int_as_float(0x7fc00000);
+            if (M == 0 && reduction != kReduceNone)  // the mean of nothing is 0/0, the sum 0
+                *loss = reduction == kReduceMean ? __int_as_float(0x7fc00000) : 0.f;
             if (any_bad)
                 atomicOr(&g_flags, kFlagBadTarget);
         }
@@ -1348,12 +1349,44 @@ __global__ void __launch_bounds__(NT) ce_count_kernel(const int64_t *targets, in
 // programmatic dependent, it waits for the row kernel to complete first).
 template <int NT>
 __global__ void __launch_bounds__(NT) ce_mean_kernel(const float *row_loss, int64_t M,
-                                                     const int *n_ptr, float *loss)
+                                                     const int *n_ptr, float *loss, int reduction)
 {
     wait_prerequisite_grid();
     const float s = sum_row_losses<NT>(row_loss, M, threadIdx.x, 1);
     if (threadIdx.x == 0)
-        *loss = s / static_cast<float>(__ldcg(n_ptr));
+        *loss = reduction == kReduceMean ? s / static_cast<float>(__ldcg(n_ptr)) : s;
+}
+
+// x[r, :N] *= scale[per_row ? r : 0], in place (Liger-Kernel cross_entropy.py,
+// element_mul, applied by LigerCrossEntropyFunction.backward when grad_output
+// is not 1).  A single scale of exactly 1 returns at once on the device, so
+// the caller needs no host-side test of grad_output.
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT) scale_rows_kernel(void *x, int64_t stride, int64_t M,
+                                                        int64_t N, const float *scale, int per_row)
+{
+    using E = Elem<T>;
+    constexpr int VEC = E::kPerVec;
+    if (!per_row && __ldg(scale) == 1.f)
+        return;
+    for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
+        const float sc = __ldg(scale + (per_row ? r : 0));
+        T *row = static_cast<T *>(x) + r * stride;
+        const RowGeom g = row_geom(row, N);
+        if (static_cast<int>(threadIdx.x) < g.head)
+            E::store(row + threadIdx.x, E::load(row + threadIdx.x) * sc);
+        if (static_cast<int>(threadIdx.x) < g.tail)
+            E::store(row + g.tail_start + threadIdx.x, E::load(row + g.tail_start + threadIdx.x) * sc);
+        uint4 *v = reinterpret_cast<uint4 *>(row + g.head);
+        for (int64_t j = threadIdx.x; j < g.nvec; j += NT) {
+            float f[VEC];
+            E::unpack(__ldcs(v + j), f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                f[e] *= sc;
+            __stcs(v + j, E::pack(f));
+        }
+    }
 }
 
 }  // namespace gbce

@@ -40,7 +40,15 @@ typedef struct CUstream_st *gbce_stream_t;
 /* Element types of the logits / softmax operands. */
 enum gbce_dtype {
     GBCE_F32 = 0,  /* IEEE binary32 */
-    GBCE_BF16 = 1  /* bfloat16; arithmetic is fp32, results are rounded to nearest even */
+    GBCE_BF16 = 1, /* bfloat16; arithmetic is fp32, results are rounded to nearest even */
+    GBCE_F16 = 2   /* IEEE binary16; arithmetic is fp32, results rounded to nearest even */
+};
+
+/* Reductions of ce_fwd_bwd_ex (PyTorch CrossEntropyLoss's reduction argument). */
+enum gbce_reduction {
+    GBCE_MEAN = 0, /* L = sum of row losses / n (n = rows whose target is not ignored) */
+    GBCE_SUM = 1,  /* L = sum of row losses */
+    GBCE_NONE = 2  /* the row losses themselves, no scalar */
 };
 
 enum gbce_status {
@@ -52,7 +60,8 @@ enum gbce_status {
     GBCE_ERR_CUDA = 5,        /* a CUDA runtime call (allocation, launch) failed */
     GBCE_ERR_BAD_TARGET = 6,  /* device flag: a target outside [0, V) that is not ignore_index */
     GBCE_ERR_TIMEOUT = 7,     /* device flag: a bounded wait on an asynchronous copy gave up */
-    GBCE_ERR_NO_DEVICE = 8    /* no usable CUDA device */
+    GBCE_ERR_NO_DEVICE = 8,   /* no usable CUDA device */
+    GBCE_ERR_REDUCTION = 9    /* reduction is not a gbce_reduction */
 };
 
 /*
@@ -86,6 +95,52 @@ enum gbce_status {
  */
 GBCE_API int ce_fwd_bwd(void *logits, int64_t stride, const int64_t *targets, float *loss, int64_t M,
                int64_t V, int64_t ignore_index, int dtype, gbce_stream_t stream);
+
+/*
+ * ce_fwd_bwd_ex -- ce_fwd_bwd with a reduction, a per-row loss output and the
+ * incoming gradient of the loss folded into the in-place gradient.
+ *
+ * Defined by: Liger-Kernel, src/liger_kernel/ops/cross_entropy.py: the kernel
+ * docstring defers to PyTorch's CrossEntropyLoss, whose reduction is 'mean',
+ * 'sum' or 'none'; LigerCrossEntropyFunction.backward multiplies the stored
+ * gradient by grad_output (element_mul).  Here that multiplication happens in
+ * the same pass that writes the gradient, when the caller knows grad_output
+ * in advance (e.g. a loss scale).
+ *
+ *   logits, stride, targets, M, V, ignore_index, dtype: as for ce_fwd_bwd;
+ *                 dtype may also be GBCE_F16.  logits is overwritten with
+ *                   g[r,i] = (softmax(x_r)_i - [i == t_r]) * k_r,
+ *                   k_r = s / n (GBCE_MEAN), s (GBCE_SUM), s_r (GBCE_NONE),
+ *                 and 0 for ignored rows.
+ *   loss          one float receiving L (GBCE_MEAN: NaN when n == 0; GBCE_SUM: 0
+ *                 when M == 0); not used, and may be NULL, for GBCE_NONE.
+ *   row_loss      M floats receiving the row losses l_r (0 for ignored rows, NaN
+ *                 for an out-of-range target), 16-byte aligned; required for
+ *                 GBCE_NONE, optional (NULL) otherwise.
+ *   grad_scale    device floats giving s: NULL means 1; one float for GBCE_MEAN
+ *                 and GBCE_SUM; M floats (s_r) for GBCE_NONE.  Read on the device.
+ *   reduction     a gbce_reduction, else GBCE_ERR_REDUCTION.
+ *
+ * ce_fwd_bwd(...) is ce_fwd_bwd_ex(..., loss, NULL, NULL, ..., GBCE_MEAN).
+ */
+GBCE_API int ce_fwd_bwd_ex(void *logits, int64_t stride, const int64_t *targets, float *loss,
+                           float *row_loss, const float *grad_scale, int64_t M, int64_t V,
+                           int64_t ignore_index, int dtype, int reduction, gbce_stream_t stream);
+
+/*
+ * scale_rows -- x[r, 0:N] *= scale[per_row ? r : 0], in place.
+ *
+ * Defined by: Liger-Kernel cross_entropy.py, element_mul as applied by
+ * LigerCrossEntropyFunction.backward to the gradient stored in place by the
+ * forward.  The page skips the call when grad_output == 1 after a host-side
+ * comparison (a synchronisation); here the kernel reads the scale on the
+ * device and returns at once when a single scale equals 1, so no host sync.
+ *
+ *   x      [M, stride] of dtype (any gbce_dtype), updated in place.
+ *   scale  device floats: one (per_row == 0) or M (per_row != 0).
+ */
+GBCE_API int scale_rows(void *x, int64_t stride, int64_t M, int64_t N, int dtype,
+                        const float *scale, int per_row, gbce_stream_t stream);
 
 /* Largest row count M that ce_fwd_bwd_noalloc accepts. */
 #define GBCE_NOALLOC_MAX_ROWS 65536

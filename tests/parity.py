@@ -11,6 +11,11 @@ bf16 (fp32 arithmetic, one round-to-nearest-even store):
   softmax:              |y - o| <= (2^-8 + 2e-5) |o| + FLOOR
   softmax backward:     |dx - o| <= (2^-8 + 1e-5) |o| + 2e-5 |y_i| sum_j |y_j dy_j| + FLOOR
   loss:                 |L - Lo| <= 1e-3 |Lo|
+fp16: as bf16 with 2^-10 in place of 2^-8 (an 11-bit significand), and an absolute
+floor of 2^-24 (the spacing of fp16 subnormals): small gradients of a large batch
+are subnormal or zero in fp16.
+A 16-bit gradient scaled after it was stored (the autograd backward) is rounded
+twice: twice the relative bound, the first floor amplified by the scale.
 FLOOR = 1e-37 covers results below fp32's normal range, which the kernels flush to zero.
 """
 import numpy as np
@@ -18,6 +23,17 @@ import torch
 
 FLOOR = 1e-37
 BF16_REL = 2.0 ** -8 + 2e-5
+F16_REL = 2.0 ** -10 + 2e-5
+F16_FLOOR = 2.0 ** -24
+
+
+def rel_floor(dtype):
+    """(relative bound of one rounding + fp32 error, absolute floor) of a stored result."""
+    if dtype == torch.float32:
+        return 1e-5, FLOOR
+    if dtype == torch.float16:
+        return F16_REL, F16_FLOOR
+    return BF16_REL, FLOOR
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
@@ -36,19 +52,37 @@ def check_grad(got: torch.Tensor, ref: np.ndarray, n: int, dtype, what="gradient
     g = to_f64(got)
     ref = np.asarray(ref, dtype=np.float64)
     assert g.shape == ref.shape
-    if dtype == torch.float32:
-        tol = 1e-5 * np.abs(ref) + FLOOR
-    else:
-        nabs = np.abs(n * g - n * ref)
-        _report(nabs > 2e-2, n * g, n * ref, np.full_like(ref, 2e-2), what + " (n*g, 2e-2)")
-        tol = BF16_REL * np.abs(ref) + FLOOR
+    check_grad_factor(got, ref, np.full(g.shape[0], 1.0 / n) if n else np.ones(g.shape[0]),
+                      dtype, what)
+
+
+def check_grad_factor(got, ref, k_rows, dtype, what="gradient", rescaled_by=None):
+    """Gradient rows (p - onehot) * k_r: for 16-bit storage the stated 2e-2 bound
+    applies to (p - onehot), i.e. |g - o| <= 2e-2 |k_r|; and the relative bound
+    of one rounding.  `rescaled_by` (per row) marks a gradient stored once and
+    then multiplied by that factor and stored again (the autograd backward): two
+    roundings, the first one's absolute floor amplified by the factor."""
+    g = to_f64(got)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert g.shape == ref.shape
+    rel, floor = rel_floor(dtype)
+    amp = 1.0
+    if rescaled_by is not None and dtype != torch.float32:
+        rel *= 2
+        amp = 1.0 + np.abs(np.asarray(rescaled_by, dtype=np.float64))[:, None]
+    if dtype != torch.float32:
+        k = np.abs(np.asarray(k_rows, dtype=np.float64))[:, None]
+        lim = 2e-2 * k + amp * floor
+        _report(~(np.abs(g - ref) <= lim), g, ref, np.broadcast_to(lim, g.shape),
+                what + " (2e-2 on p - onehot)")
+    tol = rel * np.abs(ref) + amp * floor
     _report(~(np.abs(g - ref) <= tol), g, ref, tol, what)
 
 
 def check_softmax(got: torch.Tensor, ref: np.ndarray, dtype, what="softmax"):
     y = to_f64(got)
-    rel = 1e-5 if dtype == torch.float32 else BF16_REL
-    tol = rel * np.abs(ref) + FLOOR
+    rel, floor = rel_floor(dtype)
+    tol = rel * np.abs(ref) + floor
     _report(~(np.abs(y - ref) <= tol), y, ref, tol, what)
 
 
@@ -60,7 +94,8 @@ def check_softmax_bwd(got: torch.Tensor, ref: np.ndarray, y: torch.Tensor, dy: t
     if dtype == torch.float32:
         tol = 1e-5 * (np.abs(ref) + scale) + FLOOR
     else:
-        tol = (2.0 ** -8 + 1e-5) * np.abs(ref) + 2e-5 * scale + FLOOR
+        rel, floor = rel_floor(dtype)
+        tol = (rel - 1e-5) * np.abs(ref) + 2e-5 * scale + floor
     _report(~(np.abs(dx - ref) <= tol), dx, ref, tol, what)
 
 

@@ -27,6 +27,8 @@ def lib():
     lib.ce_fwd_bwd.argtypes = [p, i64, p, p, i64, i64, i64, ci, p]
     lib.softmax_fwd.argtypes = [p, i64, p, i64, i64, i64, ci, p]
     lib.softmax_bwd.argtypes = [p, i64, p, i64, p, i64, i64, i64, ci, p]
+    lib.ce_fwd_bwd_ex.argtypes = [p, i64, p, p, p, p, i64, i64, i64, ci, ci, p]
+    lib.scale_rows.argtypes = [p, i64, i64, i64, ci, p, ci, p]
     lib.gbce_status_string.restype = ctypes.c_char_p
     return lib
 
@@ -34,7 +36,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = set(declared_functions())
     assert {"ce_fwd_bwd", "softmax_fwd", "softmax_bwd", "gbce_last_error",
-            "gbce_status_string", "gbce_timing_enable", "gbce_timing_read"} <= names
+            "gbce_status_string", "gbce_timing_enable", "gbce_timing_read", "ce_fwd_bwd_ex",
+            "scale_rows"} <= names
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -49,7 +52,7 @@ def test_only_the_abi_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(9):
+    for code in range(10):
         s = lib.gbce_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.gbce_status_string(99).decode() == "unknown status"
@@ -67,7 +70,7 @@ FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
     ((FAKE, 9, FAKE, FAKE, 4, 10, -100, 0), 2),         # stride < V
     ((FAKE, 10, FAKE, FAKE, -1, 10, -100, 0), 2),       # M < 0
     ((FAKE, 10, FAKE, FAKE, 4, 2**31, -100, 0), 2),     # V beyond int32
-    ((FAKE, 10, FAKE, FAKE, 4, 10, -100, 2), 3),        # unknown dtype
+    ((FAKE, 10, FAKE, FAKE, 4, 10, -100, 3), 3),        # unknown dtype
     ((FAKE + 2, 10, FAKE, FAKE, 4, 10, -100, 0), 4),    # fp32 logits not 4-byte aligned
     ((FAKE + 1, 10, FAKE, FAKE, 4, 10, -100, 1), 4),    # bf16 logits not 2-byte aligned
     ((FAKE, 10, FAKE + 4, FAKE, 4, 10, -100, 0), 4),    # targets not 8-byte aligned
@@ -83,6 +86,7 @@ def test_ce_rejects_bad_arguments(lib, args, code):
     ((FAKE, 8, FAKE, 7, 2, 8, 0), 2),
     ((FAKE, 8, FAKE, 8, 2, 0, 0), 2),
     ((FAKE, 8, FAKE, 8, 2, 8, 5), 3),
+    ((FAKE + 1, 8, FAKE, 8, 2, 8, 2), 4),      # fp16 x not 2-byte aligned
     ((FAKE + 2, 8, FAKE, 8, 2, 8, 0), 4),
 ])
 def test_softmax_fwd_rejects_bad_arguments(lib, args, code):
@@ -106,3 +110,34 @@ def test_empty_softmax_is_a_noop(lib):
     # M == 0 returns success without touching the device
     assert lib.softmax_fwd(None, 8, None, 8, 0, 8, 0, None) == 0
     assert lib.softmax_bwd(None, 8, None, 8, None, 8, 0, 8, 1, None) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    # (logits, stride, targets, loss, row_loss, grad_scale, M, V, ii, dtype, reduction) -> status
+    ((FAKE, 10, FAKE, FAKE, None, None, 4, 10, -100, 0, 3), 9),      # unknown reduction
+    ((FAKE, 10, FAKE, None, None, None, 4, 10, -100, 0, 0), 1),      # mean needs loss
+    ((FAKE, 10, FAKE, None, None, None, 4, 10, -100, 0, 1), 1),      # sum needs loss
+    ((FAKE, 10, FAKE, None, None, None, 4, 10, -100, 0, 2), 1),      # none needs row_loss
+    ((FAKE, 10, FAKE, FAKE, FAKE + 8, None, 4, 10, -100, 0, 0), 4),  # row_loss not 16-aligned
+    ((FAKE, 10, FAKE, FAKE, None, FAKE + 2, 4, 10, -100, 0, 0), 4),  # grad_scale not 4-aligned
+    ((FAKE, 10, FAKE, FAKE, None, None, 4, 10, -100, 5, 0), 3),      # unknown dtype
+    ((FAKE, 9, FAKE, FAKE, None, None, 4, 10, -100, 0, 0), 2),       # stride < V
+])
+def test_ce_ex_rejects_bad_arguments(lib, args, code):
+    assert lib.ce_fwd_bwd_ex(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    # (x, stride, M, N, dtype, scale, per_row) -> status
+    ((None, 8, 2, 8, 0, FAKE, 0), 1),
+    ((FAKE, 8, 2, 8, 0, None, 0), 1),
+    ((FAKE, 7, 2, 8, 0, FAKE, 0), 2),
+    ((FAKE, 8, 2, 8, 4, FAKE, 0), 3),
+    ((FAKE, 8, 2, 8, 0, FAKE + 1, 0), 4),
+])
+def test_scale_rows_rejects_bad_arguments(lib, args, code):
+    assert lib.scale_rows(*args, None) == code
+
+
+def test_empty_calls_are_noops(lib):
+    assert lib.scale_rows(None, 8, 0, 8, 0, None, 0, None) == 0

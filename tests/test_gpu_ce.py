@@ -75,7 +75,7 @@ def test_ce_deterministic():
     assert la.item() == lb.item() or (math.isnan(la.item()) and math.isnan(lb.item()))
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16], ids=str)
 @pytest.mark.parametrize("V", [1, 2, 3, 7, 8, 9, 33, 1000, 4099, 20000, 40000, 65537, 262147, 1000003])
 def test_ce_shapes_padded_and_misaligned(dtype, V):
     """Ragged V (cluster sizes 1..16 and the streaming fallback), a padded row

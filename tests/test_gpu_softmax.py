@@ -12,7 +12,7 @@ from parity import check_softmax, check_softmax_bwd
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16], ids=str)
 @pytest.mark.parametrize("N", workloads.SOFTMAX_NS)
 def test_softmax_reduced_rows(dtype, N):
     require_gpu()
@@ -43,7 +43,7 @@ def test_softmax_full_size_sampled_rows(N):
     check_softmax_bwd(got_dx[r], ref_dx, y[r], dy[r], torch.float32)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16], ids=str)
 @pytest.mark.parametrize("N", [1, 3, 7, 8, 9, 33, 1000, 65537, 300001, 1000003])
 def test_softmax_shapes_strides_and_aliasing(dtype, N):
     """Ragged N, the in-place forms (y = x, dx = dy), and operands whose rows
