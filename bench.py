@@ -160,13 +160,19 @@ class ClockSampler:
 def barrier_sync(ws):
     if ws > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+
+
+def _collective_device():
+    # NCCL reduces CUDA tensors; gloo (the CPU tests of this harness) host tensors
+    return "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
 
 
 def max_over_ranks(x: float, ws: int) -> float:
     if ws == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_collective_device())
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 
@@ -174,9 +180,16 @@ def max_over_ranks(x: float, ws: int) -> float:
 def sum_over_ranks(x: float, ws: int) -> float:
     if ws == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=_collective_device())
     torch.distributed.all_reduce(t)
     return float(t.item())
+
+
+def replica_throughput(rows_this_rank: float, ms_this_rank: float, ws: int):
+    """(rows of all ranks / slowest rank's seconds, slowest rank's ms): the
+    whole-job value of N independent replicas."""
+    ms = max_over_ranks(ms_this_rank, ws)
+    return sum_over_ranks(rows_this_rank, ws) / (ms / 1e3), ms
 
 
 # ---------------------------------------------------------------------------
@@ -352,9 +365,7 @@ def run_gbce(args, ws, rank, local):
     with ClockSampler(local) as clocks:
         total_ms, kavg_ms, loss_val = time_ce(w, xd0, td, args.steps, args.warmup, ws, flush)
     clk = clocks.summary()
-    total_ms = max_over_ranks(total_ms, ws)
-    rows_all = sum_over_ranks(float(w.M * args.steps), ws)
-    value = rows_all / (total_ms / 1e3)
+    value, total_ms = replica_throughput(float(w.M * args.steps), total_ms, ws)
     ms_per_step = total_ms / args.steps
     alg = ce_algorithmic_bytes(w, t_host)
     kavg_ms = max_over_ranks(kavg_ms, ws)

@@ -618,6 +618,23 @@ extern "C" int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int6
                                  reinterpret_cast<cudaStream_t>(stream_)));
 }
 
+extern "C" const char *gbce_plan(int op, int64_t cols, int dtype, int same_phase,
+                                 int *ctas_per_row)
+{
+    if (op < 0 || op > 2 || cols < 1 ||
+        (dtype != GBCE_F32 && dtype != GBCE_BF16 && dtype != GBCE_F16))
+        return nullptr;
+    const Plan p = make_plan(cols, elem_size(dtype), op == 2 ? 2 : 1, same_phase != 0);
+    if (ctas_per_row)
+        *ctas_per_row = p.C;
+    switch (p.kind) {
+    case Kind::Warp: return "rows_warp_kernel";
+    case Kind::Resident: return "rows_resident_kernel";
+    case Kind::Ring: return "rows_ring_kernel";
+    default: return "rows_streaming_kernel";
+    }
+}
+
 extern "C" int gbce_last_error(gbce_stream_t stream_)
 {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_));

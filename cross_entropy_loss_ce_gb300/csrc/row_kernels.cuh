@@ -1,30 +1,36 @@
 // Row kernels: fused cross-entropy forward+backward, softmax forward, softmax
-// backward.  Rows are staged in shared memory with 1-D bulk (TMA) copies so
-// that HBM sees one read and one write per element: short rows stay resident
-// in one CTA (rows_resident_kernel); longer rows stream twice through a
-// warp-specialised ring whose second read is served by L2, split across a
-// thread-block cluster when needed (rows_ring_kernel).
+// backward, in four regimes chosen on the host by the row length:
+//   rows_warp_kernel      rows of <= 4 KB per operand: one warp per row, the row
+//                         in registers;
+//   rows_resident_kernel  rows of <= 64 KB: one CTA per row, the row staged in
+//                         shared memory by 1-D bulk (TMA) copies;
+//   rows_ring_kernel      longer rows: persistent, a producer warp streams each
+//                         row twice through a shared-memory ring (the second
+//                         read served by L2), split across a thread-block
+//                         cluster when the rows between reads would not fit L2;
+//   rows_streaming_kernel operands whose rows start at different 16-byte
+//                         phases: element loads from global memory.
+// HBM sees one read and one write per element in the first three.
 //
 // Per row (cross-entropy; the softmax forward is the same without the target):
 //   1. target load and ignore test (Liger-Kernel cross_entropy.py,
 //      liger_cross_entropy_kernel, steps 1-2).  Ignored rows are zero-filled
 //      with no read; a target outside [0, V) raises a flag and leaves the row.
 //   2. pass 1, the online normaliser (same kernel, step 3, "Algorithm 3" of
-//      the online-softmax paper it cites): each thread takes the max m of its
-//      elements, then d = sum exp(x - m); the (m, d) pairs are merged by warp
-//      shuffles, through shared memory, then across the cluster over
-//      distributed shared memory, rescaling each sum to the larger max.
-//   3. pass 2, the gradient in place (step 4 and step 6):
-//      g_i = exp(x_i - M) / (D n), and (exp(x_y - M)/D - 1)/n at the target,
-//      computed from the staged copy, so the second pass does not touch HBM.
-//   4. the row loss M + ln D - x_y (step 5), x_y captured before any store.
+//      the online-softmax paper it cites): running maxima m and rescaled sums
+//      d = sum exp(x - m), merged as (m, d) pairs by warp shuffles, through
+//      shared memory, and across a cluster, each sum rescaled to the larger max.
+//   3. pass 2, the gradient in place (steps 4 and 6): exp(x_i - M) / D times
+//      the row's factor k (1/n for the mean), and (exp(x_y - M) / D - 1) k at
+//      the target, written from the staged copy or registers.
+//   4. the row loss M + ln D - x_y (step 5), x_y read before any store.
 #pragma once
 
 #include "device.cuh"
 
 namespace gbce {
 
-constexpr int kMaxChunks = 8;  // bulk copies (one mbarrier each) per CTA slice
+constexpr int kMaxChunks = 8;  // bulk copies (one mbarrier each) per staged row
 
 enum class Op { CE, SoftmaxFwd, SoftmaxBwd };
 
@@ -47,10 +53,10 @@ struct RowArgs {
     int reduction;      // kReduceMean / kReduceSum / kReduceNone
     const float *grad_scale;  // NULL (1), one value, or one per row (kReduceNone)
     // launch plan
-    int C;          // CTAs per row (cluster size)
-    int per_vec;    // 16-byte vectors per CTA slice (capacity of one staged buffer)
-    int chunk_vec;  // vectors per bulk copy, a multiple of the CTA's thread count
-    int nslot;      // ring slots (ring kernel)
+    int C;          // CTAs per row (cluster size; ring and streaming kernels)
+    int per_vec;    // resident: 16-byte vectors staged per operand
+    int chunk_vec;  // resident: vectors per bulk copy, a multiple of the thread count
+    int nslot;      // ring: slots of the shared-memory ring
 };
 
 // Sticky error flags of this device (kFlag* bits); defined once per library.

@@ -201,6 +201,19 @@ GBCE_API int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int64_
                 int64_t dx_stride, int64_t M, int64_t N, int dtype, gbce_stream_t stream);
 
 /*
+ * gbce_plan -- the row-kernel family a call uses for rows of `cols` elements
+ * of `dtype` on the current device: "rows_warp_kernel" (rows of at most 4 KB
+ * per operand, one warp per row), "rows_resident_kernel" (at most 64 KB
+ * staged per row, one CTA per row), "rows_ring_kernel" (longer rows streamed
+ * through a shared-memory ring, *ctas_per_row CTAs of a cluster per row) or
+ * "rows_streaming_kernel" (operands whose rows start at different addresses
+ * mod 16 bytes: same_phase == 0).  op: 0 ce_fwd_bwd / ce_fwd_bwd_ex,
+ * 1 softmax_fwd, 2 softmax_bwd.  Returns NULL for invalid arguments.  For
+ * tests and diagnostics; no kernel is launched.
+ */
+GBCE_API const char *gbce_plan(int op, int64_t cols, int dtype, int same_phase, int *ctas_per_row);
+
+/*
  * gbce_last_error -- synchronise `stream`, then read and clear the current
  * device's sticky error flags.  Returns GBCE_OK, GBCE_ERR_BAD_TARGET,
  * GBCE_ERR_TIMEOUT (when both are set, BAD_TARGET), or GBCE_ERR_CUDA when the

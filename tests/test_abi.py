@@ -141,3 +141,31 @@ def test_scale_rows_rejects_bad_arguments(lib, args, code):
 
 def test_empty_calls_are_noops(lib):
     assert lib.scale_rows(None, 8, 0, 8, 0, None, 0, None) == 0
+
+
+def test_plan_picks_the_regime_by_row_length(lib):
+    """Host-side plan (no device here, so no cluster split): warp rows up to
+    4 KB per operand, resident up to 64 KB staged, ring beyond, streaming when
+    operands' rows sit at different 16-byte phases."""
+    lib.gbce_plan.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                              ctypes.POINTER(ctypes.c_int)]
+    lib.gbce_plan.restype = ctypes.c_char_p
+    c = ctypes.c_int()
+
+    def plan(op, cols, dtype, same=1):
+        return lib.gbce_plan(op, cols, dtype, same, ctypes.byref(c)).decode()
+
+    assert plan(0, 1000, 0) == "rows_warp_kernel"          # 4000 B fp32
+    assert plan(0, 1024, 0) == "rows_warp_kernel"          # exactly 4 KB
+    assert plan(0, 1028, 0) == "rows_resident_kernel"
+    assert plan(0, 32000, 1) == "rows_resident_kernel"     # 64000 B bf16
+    assert plan(0, 32768, 1) == "rows_resident_kernel"     # exactly 64 KB
+    assert plan(0, 32776, 1) == "rows_ring_kernel"
+    assert plan(2, 8192, 0) == "rows_resident_kernel"      # two 32 KB operands: 64 KB
+    assert plan(2, 8196, 0) == "rows_ring_kernel"
+    assert plan(1, 8192, 0) == "rows_resident_kernel"
+    assert plan(1, 8192, 0, same=0) == "rows_streaming_kernel"
+    assert plan(0, 128256, 2) == "rows_ring_kernel"        # fp16
+    assert lib.gbce_plan(3, 10, 0, 1, None) is None
+    assert lib.gbce_plan(0, 0, 0, 1, None) is None
+    assert lib.gbce_plan(0, 10, 7, 1, None) is None

@@ -165,3 +165,20 @@ def test_ce_single_row_and_spike():
         assert status == gbce.OK
         check_grad(xd, ref["grad"], 1, torch.bfloat16)
         check_loss(loss, float(ref["row_loss"][0]), torch.bfloat16)
+
+
+def test_every_regime_is_exercised():
+    """The shapes above reach every row-kernel family on this device,
+    including the ring split across a cluster."""
+    require_gpu()
+    assert gbce.plan("ce", 1000, torch.float32)[0] == "rows_warp_kernel"
+    assert gbce.plan("ce", 4099, torch.float32)[0] == "rows_resident_kernel"
+    assert gbce.plan("ce", 65537, torch.bfloat16) == ("rows_ring_kernel", 1)
+    name, c = gbce.plan("ce", 262147, torch.float32)
+    assert name == "rows_ring_kernel" and c >= 2
+    name, c = gbce.plan("ce", 1000003, torch.float32)
+    assert name == "rows_ring_kernel" and c >= 8
+    name, c = gbce.plan("ce", 250007, torch.float32)  # the large-vocabulary fp32 workload
+    assert name == "rows_ring_kernel" and c >= 2
+    assert gbce.plan("softmax_fwd", 1000, torch.float32, same_phase=False)[0] == \
+        "rows_streaming_kernel"
