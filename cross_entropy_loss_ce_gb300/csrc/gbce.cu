@@ -27,7 +27,7 @@ constexpr int64_t kRingBytes = 192 * 1024;    // ring capacity per CTA (one CTA 
 constexpr int kRingWarps = 16;                // consumer warps of the ring kernel
 constexpr int kRingVpt1 = 4;                  // vectors per consumer thread and slot, one operand
 constexpr int kRingVpt2 = 2;                  // the same, two operands (softmax backward)
-constexpr int64_t kL2Budget = 48ll << 20;     // bytes of rows between their two reads, all SMs
+constexpr int64_t kL2Budget = 56ll << 20;     // bytes of rows between their two reads, all SMs
 
 size_t elem_size(int dtype) { return dtype == GBCE_F32 ? 4 : 2; }
 
@@ -63,6 +63,7 @@ struct Plan {
     int per_vec;    // resident: 16-byte vectors staged per operand
     int chunk_vec;  // resident: vectors per bulk copy; ring: vectors per slot
     int nslot;      // ring: slots
+    bool hold;      // ring: every slice fits half the ring and is loaded once
     size_t smem;    // dynamic shared memory per CTA
 };
 
@@ -111,7 +112,7 @@ Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned)
     const int64_t sms = current_sm_count();
     p.C = 1;
     while (p.C < kMaxCluster && sms * row_bytes * nbuf / p.C > kL2Budget)
-        p.C *= 2;
+        ++p.C;
     p.nt = (kRingWarps + 1) * 32;
     const int vpt = nbuf == 2 ? kRingVpt2 : kRingVpt1;
     const int64_t chunk_bytes = static_cast<int64_t>(kRingWarps) * 32 * vpt * 16;
@@ -120,6 +121,10 @@ Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned)
     if (p.nslot > kRingMaxSlots)
         p.nslot = kRingMaxSlots;
     p.smem = static_cast<size_t>(p.nslot) * chunk_bytes * nbuf;
+    // the most chunks any row slice needs: rows with a head have fewer vectors
+    const int64_t per_max = (nvec + p.C - 1) / p.C;
+    const int64_t nch_max = (per_max + p.chunk_vec - 1) / p.chunk_vec;
+    p.hold = 2 * nch_max <= p.nslot;
     return p;
 }
 
@@ -141,8 +146,14 @@ KernelFn pick_kernel(const Plan &p)
         }
     case Kind::Resident:
         return p.nt == 128 ? rows_resident_kernel<OP, T, 128> : rows_resident_kernel<OP, T, 256>;
-    case Kind::Ring:
-        return rows_ring_kernel<OP, T, kRingWarps, OP == Op::SoftmaxBwd ? kRingVpt2 : kRingVpt1>;
+    case Kind::Ring: {
+        constexpr int vpt = OP == Op::SoftmaxBwd ? kRingVpt2 : kRingVpt1;
+        if (p.C > 1)
+            return p.hold ? rows_ring_kernel<OP, T, kRingWarps, vpt, true, true>
+                          : rows_ring_kernel<OP, T, kRingWarps, vpt, true, false>;
+        return p.hold ? rows_ring_kernel<OP, T, kRingWarps, vpt, false, true>
+                      : rows_ring_kernel<OP, T, kRingWarps, vpt, false, false>;
+    }
     default:
         return rows_streaming_kernel<OP, T, 512>;
     }

@@ -703,7 +703,11 @@ constexpr int kRingMaxSlots = 32;
 
 constexpr int kRingMaxCluster = 16;
 
-template <Op OP, typename T, int NCW, int VPT>
+// CLUSTER: rows are split across a cluster of a.C CTAs (else one CTA per row).
+// HOLD: every row slice fills at most half the ring and is loaded once, held
+// for pass 2 (the host checks this bound for the whole launch).  Both are
+// template parameters so that the common path carries no code of the other.
+template <Op OP, typename T, int NCW, int VPT, bool CLUSTER, bool HOLD>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowArgs a)
 {
     using E = Elem<T>;
@@ -725,8 +729,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const int C = a.C;
-    const int rank = C > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int C = CLUSTER ? a.C : 1;
+    const int rank = CLUSTER ? static_cast<int>(cluster_rank()) : 0;
     const int64_t cid = blockIdx.x / C;
     const int64_t G = gridDim.x / C;
     const int nslot = a.nslot;
@@ -742,7 +746,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
         fence_barrier_init();
     }
     __syncthreads();
-    if (C > 1) {  // every peer's barriers exist before anyone signals them
+    if constexpr (CLUSTER) {  // every peer's barriers exist before anyone signals them
         cluster_arrive_any();
         cluster_wait_any();
     }
@@ -770,12 +774,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                 const int64_t cnt = v0 < g.nvec ? (v0 + per < g.nvec ? per : g.nvec - v0) : 0;
                 const int64_t body = g.head + v0 * VEC;
                 const int64_t nch = (cnt + CHUNK - 1) / CHUNK;
-                // a slice that fills at most half the ring stays resident for both passes
-                const int passes = 2 * nch <= nslot ? 1 : 2;
+                if (HOLD && 2 * nch > nslot)
+                    continue;  // outside the launch's bound: the consumers skip it too
+                // a held slice is loaded once; otherwise the row is streamed twice
+                constexpr int passes = HOLD ? 1 : 2;
                 for (int pass = 0; pass < passes && ok; ++pass) {
                     for (int64_t kk = 0; kk < nch; ++kk) {
-                        const int64_t k = pass == 0 ? kk : nch - 1 - kk;
-                        const int64_t c0 = k * CHUNK;
+                        const int64_t c0 = kk * CHUNK;
                         const int64_t c1 = c0 + CHUNK < cnt ? c0 + CHUNK : cnt;
                         const uint32_t bytes = static_cast<uint32_t>(c1 - c0) * 16u;
                         if (!mbar_wait_bounded(smem_addr(&empty[slot]), ph ^ 1u)) {
@@ -850,7 +855,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                 }
             }
             const int64_t nch = (cnt + CHUNK - 1) / CHUNK;
-            const bool hold = 2 * nch <= nslot;  // loaded once, kept for pass 2
+            if (HOLD && 2 * nch > nslot) {  // cannot happen for a valid plan: flag, skip
+                if (tid == 0) {
+                    atomicOr(&g_flags, kFlagTimeout);
+                    if (OP == Op::CE && rank == 0)
+                        a.row_loss[row] = __int_as_float(0x7fc00000);
+                }
+                continue;
+            }
+            constexpr bool hold = HOLD;  // loaded once, kept for pass 2
             const uint32_t slot0 = slot, ph0 = ph;
             float h0 = 0.f, h1 = 0.f, t0 = 0.f, t1 = 0.f;
             if (head_here) {
@@ -1018,7 +1031,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
             // ---- merge across the cluster: each CTA sends its partial to every
             // peer's slot (st.async, counted on the peer's exchange barrier) and
             // folds the C partials in rank order, so all CTAs get the same bits.
-            if (C > 1) {
+            if constexpr (CLUSTER) {
                 const int pi = live & 1;
                 if (tid == 0) {
                     asm volatile("" ::"f"(xy));  // the target logit was read before peers store
@@ -1046,7 +1059,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
             }
             ++live;
 
-            // ---- pass 2: the slice again, chunks in reverse order
+            // ---- pass 2: the slice again (the same slots when held, else a
+            // second read that L2 serves), chunks in order
             float scale = 0.f, sub = 0.f, ML = 0.f;
             if constexpr (OP != Op::SoftmaxBwd) {
                 ML = r.x * kLog2e;
@@ -1062,8 +1076,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                 ph = ph0;
             }
             for (int64_t kk = 0; kk < nch; ++kk) {
-                const int64_t k = hold ? kk : nch - 1 - kk;
-                const int64_t c0 = k * CHUNK;
+                const int64_t c0 = kk * CHUNK;
                 const int cn = static_cast<int>((c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0);
                 if (ok && !hold)
                     ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[slot]), ph));
@@ -1162,7 +1175,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
             }
         }
     }
-    if (C > 1) {  // no CTA leaves while a peer may still signal it
+    if constexpr (CLUSTER) {  // no CTA leaves while a peer may still signal it
         cluster_arrive_any();
         cluster_wait_any();
     }
