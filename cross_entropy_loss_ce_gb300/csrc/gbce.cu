@@ -13,8 +13,6 @@
 #include "row_kernels.cuh"
 
 namespace gbce {
-
-
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -212,6 +210,8 @@ cudaMemPool_t g_pool[kMaxDevices] = {};
 
 cudaError_t pool_for(int device, cudaMemPool_t *out)
 {
+    if (device < 0 || device >= kMaxDevices)
+        return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_pool_mu);
     if (!g_pool[device]) {
         cudaMemPoolProps props = {};
@@ -246,7 +246,8 @@ cudaEvent_t take_event()
         return e;
     }
     cudaEvent_t e = nullptr;
-    cudaEventCreate(&e);
+    if (cudaEventCreate(&e) != cudaSuccess)
+        return nullptr;
     return e;
 }
 
@@ -259,7 +260,13 @@ struct TimedRegion {
             std::lock_guard<std::mutex> lk(g_timing_mu);
             start = take_event();
             stop = take_event();
-            cudaEventRecord(start, stream);
+            if (!start || !stop || cudaEventRecord(start, stream) != cudaSuccess) {
+                if (start)
+                    g_event_free.push_back(start);
+                if (stop)
+                    g_event_free.push_back(stop);
+                start = stop = nullptr;  // this call goes untimed
+            }
         }
     }
     ~TimedRegion()
@@ -379,12 +386,15 @@ cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a, cudaStream
 
 // Largest row count such that M * C fits a 1-D grid.
 constexpr int64_t kMaxRows = (int64_t{1} << 31) / kMaxCluster - 1;
+// Largest row stride in elements: keeps row * stride * element size far from
+// int64 overflow (no device has 2^48 bytes).
+constexpr int64_t kMaxStride = int64_t{1} << 46;
 
 int check_matrix(const void *p, int64_t stride, int64_t M, int64_t cols, int dtype)
 {
     if (M > 0 && !p)
         return GBCE_ERR_NULL;
-    if (stride < cols)
+    if (stride < cols || stride > kMaxStride)
         return GBCE_ERR_SIZE;
     if (!aligned_to(p, elem_size(dtype)))
         return GBCE_ERR_ALIGN;

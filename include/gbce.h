@@ -10,8 +10,9 @@
  *
  * Layout: a matrix argument is M rows of `cols` elements, row r starting at
  * element r * stride of the pointer (row-major, unit column stride, stride in
- * ELEMENTS, stride >= cols).  Columns at and beyond `cols` are never read or
- * written.  Row offsets are computed in 64-bit arithmetic.
+ * ELEMENTS, cols <= stride <= 2^46; M <= 2^27 - 1; cols < 2^31).  Columns at
+ * and beyond `cols` are never read or written.  Row offsets are computed in
+ * 64-bit arithmetic.
  *
  * Return value: GBCE_OK (0) or a gbce_status code.  Argument errors are
  * detected on the host before anything is launched and leave every buffer

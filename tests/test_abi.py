@@ -169,3 +169,10 @@ def test_plan_picks_the_regime_by_row_length(lib):
     assert lib.gbce_plan(3, 10, 0, 1, None) is None
     assert lib.gbce_plan(0, 0, 0, 1, None) is None
     assert lib.gbce_plan(0, 10, 7, 1, None) is None
+
+
+def test_size_limits(lib):
+    # stride beyond 2^46 elements and M beyond 2^27 - 1 rows are rejected on the host
+    assert lib.ce_fwd_bwd(FAKE, 2 ** 47, FAKE, FAKE, 4, 10, -100, 0, None) == 2
+    assert lib.ce_fwd_bwd(FAKE, 10, FAKE, FAKE, 2 ** 27, 10, -100, 0, None) == 2
+    assert lib.softmax_fwd(FAKE, 2 ** 47, FAKE, 8, 2, 8, 0, None) == 2
