@@ -1,0 +1,71 @@
+"""Calls on several streams at once, and a CUDA graph capturing ce_fwd_bwd
+(stream-ordered scratch, programmatic dependent launches) replayed on new inputs."""
+import numpy as np
+import pytest
+import torch
+
+import cross_entropy_loss_ce_gb300 as gbce
+import oracle
+import workloads
+from gpu_util import oracle_ce, require_gpu
+from parity import check_grad, check_loss
+
+pytestmark = pytest.mark.gpu
+II = workloads.IGNORE_INDEX
+
+
+def _case(M, V, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn((M, V), generator=g) * 2).to(dtype)
+    t = torch.randint(0, V, (M,), generator=g)
+    t[::7] = II
+    return x, t
+
+
+def test_concurrent_calls_on_two_streams():
+    require_gpu()
+    cases = [_case(64, 50000, torch.bfloat16, 1), _case(96, 3000, torch.float32, 2),
+             _case(32, 200000, torch.float32, 3)]
+    refs = [oracle_ce(x, t) for x, t in cases]
+    streams = [torch.cuda.Stream() for _ in cases]
+    devs = [(x.cuda(), t.cuda()) for x, t in cases]
+    torch.cuda.synchronize()
+    losses = []
+    for s, (xd, td) in zip(streams, devs):
+        with torch.cuda.stream(s):
+            losses.append(gbce.ce_fwd_bwd(xd, td, II))
+    torch.cuda.synchronize()
+    assert gbce.last_error() == gbce.OK
+    for (x, t), (xd, td), ref, loss in zip(cases, devs, refs, losses):
+        check_grad(xd, ref["grad"], ref["n"], x.dtype)
+        check_loss(float(loss.item()), oracle.ce_mean(ref["row_loss"], ref["n"]), x.dtype)
+
+
+@pytest.mark.parametrize("V", [1000, 32000, 128256])  # warp, resident, ring
+def test_graph_capture_and_replay(V):
+    require_gpu()
+    M = 64
+    x0, t0 = _case(M, V, torch.bfloat16, V)
+    x1, t1 = _case(M, V, torch.bfloat16, V + 1)
+    xd = torch.empty((M, V), dtype=torch.bfloat16, device="cuda")
+    td = torch.empty((M,), dtype=torch.int64, device="cuda")
+    loss = torch.empty((), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        xd.copy_(x0.cuda())
+        td.copy_(t0.cuda())
+        gbce.ce_fwd_bwd(xd, td, II, loss)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gbce.ce_fwd_bwd(xd, td, II, loss)
+    for x, t in ((x0, t0), (x1, t1), (x0, t0)):
+        xd.copy_(x.cuda())
+        td.copy_(t.cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = oracle_ce(x, t)
+        check_grad(xd, ref["grad"], ref["n"], torch.bfloat16, f"graph replay V={V}")
+        check_loss(float(loss.item()), oracle.ce_mean(ref["row_loss"], ref["n"]), torch.bfloat16)
+    assert gbce.last_error() == gbce.OK
