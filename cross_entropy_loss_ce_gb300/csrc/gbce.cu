@@ -16,7 +16,7 @@ namespace gbce {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kWarpMaxVpl = 8;                // rows of <= 32 * 8 16-byte vectors: warp kernel
+constexpr int kWarpMaxVpl = 16;               // rows of <= 32 * 16 16-byte vectors: warp kernel
 constexpr int64_t kResidentMax = 64 * 1024;   // rows up to this many staged bytes: resident kernel
 constexpr int64_t kSliceMax = 200 * 1024;     // dynamic shared memory limit set on every kernel
 constexpr int kMaxCluster = 16;
@@ -140,7 +140,8 @@ KernelFn pick_kernel(const Plan &p)
         case 1: return rows_warp_kernel<OP, T, 1>;
         case 2: return rows_warp_kernel<OP, T, 2>;
         case 4: return rows_warp_kernel<OP, T, 4>;
-        default: return rows_warp_kernel<OP, T, 8>;
+        case 8: return rows_warp_kernel<OP, T, 8>;
+        default: return rows_warp_kernel<OP, T, 16>;
         }
     case Kind::Resident:
         return p.nt == 128 ? rows_resident_kernel<OP, T, 128> : rows_resident_kernel<OP, T, 256>;

@@ -1,6 +1,6 @@
 // Row kernels: fused cross-entropy forward+backward, softmax forward, softmax
 // backward, in four regimes chosen on the host by the row length:
-//   rows_warp_kernel      rows of <= 4 KB per operand: one warp per row, the row
+//   rows_warp_kernel      rows of <= 8 KB per operand: one warp per row, the row
 //                         in registers;
 //   rows_resident_kernel  rows of <= 64 KB: one CTA per row, the row staged in
 //                         shared memory by 1-D bulk (TMA) copies;

@@ -203,7 +203,7 @@ GBCE_API int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int64_
 
 /*
  * gbce_plan -- the row-kernel family a call uses for rows of `cols` elements
- * of `dtype` on the current device: "rows_warp_kernel" (rows of at most 4 KB
+ * of `dtype` on the current device: "rows_warp_kernel" (rows of at most 8 KB
  * per operand, one warp per row), "rows_resident_kernel" (at most 64 KB
  * staged per row, one CTA per row), "rows_ring_kernel" (longer rows streamed
  * through a shared-memory ring, *ctas_per_row CTAs of a cluster per row) or

@@ -145,7 +145,7 @@ def test_empty_calls_are_noops(lib):
 
 def test_plan_picks_the_regime_by_row_length(lib):
     """Host-side plan (no device here, so no cluster split): warp rows up to
-    4 KB per operand, resident up to 64 KB staged, ring beyond, streaming when
+    8 KB per operand, resident up to 64 KB staged, ring beyond, streaming when
     operands' rows sit at different 16-byte phases."""
     lib.gbce_plan.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                               ctypes.POINTER(ctypes.c_int)]
@@ -156,8 +156,8 @@ def test_plan_picks_the_regime_by_row_length(lib):
         return lib.gbce_plan(op, cols, dtype, same, ctypes.byref(c)).decode()
 
     assert plan(0, 1000, 0) == "rows_warp_kernel"          # 4000 B fp32
-    assert plan(0, 1024, 0) == "rows_warp_kernel"          # exactly 4 KB
-    assert plan(0, 1028, 0) == "rows_resident_kernel"
+    assert plan(0, 2048, 0) == "rows_warp_kernel"          # exactly 8 KB
+    assert plan(0, 2052, 0) == "rows_resident_kernel"
     assert plan(0, 32000, 1) == "rows_resident_kernel"     # 64000 B bf16
     assert plan(0, 32768, 1) == "rows_resident_kernel"     # exactly 64 KB
     assert plan(0, 32776, 1) == "rows_ring_kernel"
