@@ -105,3 +105,19 @@ def check_loss(got: float, ref: float, dtype, what="loss"):
         assert np.isnan(got), f"{what}: got {got}, want NaN"
         return
     assert abs(got - ref) <= rel * abs(ref), f"{what}: got {got!r} want {ref!r} (rel {rel})"
+
+
+def ulp_distance_16(got: torch.Tensor, ref: np.ndarray, dtype) -> np.ndarray:
+    """Per element, how many representable 16-bit values (bf16 or fp16) lie
+    between the stored result and the oracle's value rounded to that format
+    (0 = correctly rounded).  Sign-magnitude bit patterns are mapped onto a
+    monotonic integer line, so +0 and -0 coincide."""
+    want = torch.from_numpy(np.asarray(ref, dtype=np.float64)).to(torch.float32).to(dtype)
+    a = got.detach().cpu().to(dtype).contiguous().view(torch.int16).numpy().astype(np.int32)
+    b = want.contiguous().view(torch.int16).numpy().astype(np.int32)
+
+    def line(v):
+        mag = v & 0x7FFF
+        return np.where(v & 0x8000, -mag, mag)
+
+    return np.abs(line(a) - line(b))

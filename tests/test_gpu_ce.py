@@ -9,7 +9,7 @@ import cross_entropy_loss_ce_gb300 as gbce
 import oracle
 import workloads
 from gpu_util import host, oracle_ce, require_gpu
-from parity import check_grad, check_loss, to_f64
+from parity import check_grad, check_loss, to_f64, ulp_distance_16
 
 pytestmark = pytest.mark.gpu
 II = workloads.IGNORE_INDEX
@@ -38,6 +38,11 @@ def test_ce_reduced_rows_all_elements(name):
     assert status == gbce.OK
     check_grad(xd, ref["grad"], ref["n"], w.dtype, f"{name} gradient")
     check_loss(loss, ref_loss, w.dtype, f"{name} loss")
+    if w.dtype != torch.float32:
+        # fp32 arithmetic then one rounding: at most one bf16 step from the
+        # correctly rounded value (off by one only next to a rounding midpoint)
+        ulps = ulp_distance_16(xd, ref["grad"], w.dtype)
+        assert ulps.max() <= 1, f"{name}: {int((ulps > 1).sum())} elements > 1 ulp"
 
 
 @pytest.mark.parametrize("name", [n for n in workloads.CE_WORKLOADS if n != "ce_f32_64x1000"])
@@ -182,3 +187,37 @@ def test_every_regime_is_exercised():
     assert name == "rows_ring_kernel" and c >= 2
     assert gbce.plan("softmax_fwd", 1000, torch.float32, same_phase=False)[0] == \
         "rows_streaming_kernel"
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=str)
+def test_ignore_index_is_a_class_id(dtype):
+    """ignore_index may be any int64: here class 0 itself, and 5."""
+    require_gpu()
+    for ii in (0, 5):
+        g = torch.Generator().manual_seed(ii)
+        x = torch.randn((40, 777), generator=g).to(dtype)
+        t = torch.randint(0, 8, (40,), generator=g)
+        ref = oracle_ce(x, t, ignore_index=ii)
+        assert ref["n"] < 40
+        xd = x.cuda()
+        loss = gbce.ce_fwd_bwd(xd, t.cuda(), ii)
+        assert gbce.last_error() == gbce.OK
+        check_grad(xd, ref["grad"], ref["n"], dtype, f"ignore_index={ii}")
+        check_loss(float(loss.item()), oracle.ce_mean(ref["row_loss"], ref["n"]), dtype)
+        assert bool((xd[t.cuda() == ii] == 0).all())
+
+
+def test_other_negative_ignore_index():
+    """With ignore_index = -1, a -100 target is out of range: flagged, its row kept."""
+    require_gpu()
+    x = torch.randn((6, 300))
+    t = torch.tensor([3, -1, -100, 299, -1, 0])
+    ref = oracle_ce(x, t, ignore_index=-1)
+    assert ref["bad"] == 1 and ref["n"] == 4
+    xd = x.cuda()
+    loss = gbce.ce_fwd_bwd(xd, t.cuda(), -1)
+    assert gbce.last_error() == gbce.ERR_BAD_TARGET
+    assert math.isnan(float(loss.item()))
+    assert torch.equal(xd[2].cpu(), x[2])
+    keep = [0, 1, 3, 4, 5]
+    check_grad(xd[keep], ref["grad"][keep], ref["n"], torch.float32, "ignore_index=-1")
