@@ -83,6 +83,8 @@ class Oracle:
         lib.oracle_widen.argtypes = [p, ci, i64, p]
         lib.oracle_softmax_fwd_rows.argtypes = [p, ci, i64, i64, p, i64, p, ci]
         lib.oracle_softmax_bwd_rows.argtypes = [p, i64, p, i64, ci, i64, p, i64, p, ci]
+        lib.oracle_softmax_bwd_bsr.argtypes = [p, i64, p, i64, ci, p, i64, i64, i64, i64, i64,
+                                               i64, ctypes.c_double, p, i64, p, i64, p]
         self.lib = lib
 
     def ce_count(self, targets, V: int, ignore_index: int = -100):
@@ -195,6 +197,38 @@ class Oracle:
             raise ValueError("oracle_softmax_bwd_rows rejected its arguments")
         return dx
 
+    def softmax_bwd_bsr(self, y: np.ndarray, dy: np.ndarray, lut, n_block_rows: int,
+                        nblocks: int, block: int, sizemax: int, scale: float = 1.0,
+                        block_rows=None):
+        """Block-sparse softmax backward: (dx, bad).
+
+        ``y`` and ``dy`` are [Z, zstride] arrays (unit inner stride) whose first
+        nblocks * block^2 elements per batch item hold the blocks; ``lut`` is
+        the int32 table.  ``dx`` is [Z, nblocks * block^2] float64: the results
+        at the positions the table names (only the listed ``block_rows`` when
+        given), the widened ``dy`` elsewhere.  ``bad`` counts the block-rows the
+        table describes wrongly (left as ``dy``).
+        """
+        code = _dtype_code(y)
+        if _dtype_code(dy) != code or y.shape[0] != dy.shape[0] or y.ndim != 2 or dy.ndim != 2:
+            raise TypeError("y and dy must be [Z, zstride] arrays of one dtype")
+        Z = y.shape[0]
+        L = nblocks * block * block
+        if y.shape[1] < L or dy.shape[1] < L:
+            raise ValueError("y and dy hold fewer than nblocks * block^2 elements per item")
+        t = np.ascontiguousarray(lut, dtype=np.int32)
+        if block_rows is not None:
+            block_rows = np.ascontiguousarray(block_rows, dtype=np.int64)
+        dx = np.ascontiguousarray(self.widen(np.ascontiguousarray(dy[:, :L])).reshape(Z, L))
+        bad = ctypes.c_int64()
+        rc = self.lib.oracle_softmax_bwd_bsr(
+            _ptr(y), _row_stride(y), _ptr(dy), _row_stride(dy), code, _ptr(t), t.size,
+            n_block_rows, nblocks, block, sizemax, Z, float(scale), _ptr(block_rows),
+            0 if block_rows is None else block_rows.size, _ptr(dx), L, ctypes.byref(bad))
+        if rc != 0:
+            raise ValueError("oracle_softmax_bwd_bsr rejected its arguments")
+        return dx, bad.value
+
 
 _default = None
 
@@ -241,3 +275,7 @@ def widen(*a, **k):
 
 def softmax_bwd(*a, **k):
     return get().softmax_bwd(*a, **k)
+
+
+def softmax_bwd_bsr(*a, **k):
+    return get().softmax_bwd_bsr(*a, **k)

@@ -33,6 +33,9 @@
  *     softmax_kernel: y = exp(x - max x) / sum exp(x - max x) per row.
  *   - same page, _backward (block-sparse softmax backward), dense math with
  *     scale 1: dx = y * (dy - sum(y * dy)).
+ *   - same page, _backward with its look-up table: the rows of a block-sparse
+ *     matrix are gathered through the table and the result is multiplied by
+ *     `scale`; see oracle_softmax_bwd_bsr below.
  *   - Liger-Kernel, LigerCrossEntropyFunction.backward and element_mul: the
  *     stored gradient is multiplied by the incoming grad_output when that is
  *     not 1.
@@ -396,4 +399,102 @@ int oracle_softmax_bwd_rows(const void *y, int64_t y_stride, const void *dy, int
     j.nrows = nrows;
     j.out = dx;
     return run_parallel(&j, nthreads);
+}
+
+/* Block-sparse softmax backward ("python sum function examples
+ * (triton.language)", _backward): the softmax output y and the upstream
+ * gradient dy of a block-sparse matrix, stored block by block.
+ *
+ * Storage: batch item z starts at z * zstride elements; block b of it holds a
+ * block x block tile, row-major, at b * block^2.  The table `lut` (int32)
+ * starts with one (size, offset) pair per block-row rbm; the row's blocks are
+ * lut[offset + 4 * rbn] for rbn = 0 .. size-1 (the other three ints of each
+ * entry are not read here).  Row pidhm = rbm * block + rxm of the matrix is
+ * the concatenation, over rbn, of row rxm of those blocks.  For each batch
+ * item and each row:
+ *
+ *   s    = sum over the row's elements of y * dy
+ *   dx_i = y_i * (dy_i - s) * scale
+ *
+ * dx (Z x zstride doubles, filled by the caller) receives the results at the
+ * positions the table names; other positions are left as they are.
+ *
+ * Readings where the page is silent: a block-row whose size is negative or
+ * above sizemax, whose entries run outside the table, or that names a block
+ * outside [0, nblocks) is bad: none of its rows is written, for any batch
+ * item, and it is counted in *bad.  A size of 0 writes nothing.
+ * block_rows (NULL: all n_block_rows) lists the block-rows to compute. */
+/* Element rxn of row rxm of block `blockid`: blocks are block x block tiles,
+ * row-major, one after another. */
+static int64_t bsr_index(int64_t blockid, int64_t rxm, int64_t rxn, int64_t block)
+{
+    return blockid * block * block + rxm * block + rxn;
+}
+
+/* The block id of entry rbn of a block-row whose entries start at `offset`:
+ * each entry is 4 ints, the block id first. */
+static int64_t bsr_block_id(const int32_t *lut, int64_t offset, int64_t rbn)
+{
+    return lut[offset + 4 * rbn];
+}
+
+int oracle_softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy, int64_t dy_zstride,
+                           int dtype, const int32_t *lut, int64_t lut_len, int64_t n_block_rows,
+                           int64_t nblocks, int64_t block, int64_t sizemax, int64_t Z,
+                           double scale, const int64_t *block_rows, int64_t n_listed,
+                           double *dx, int64_t dx_zstride, int64_t *bad)
+{
+    if (!y || !dy || !dx || !lut || !bad || block < 1 || Z < 0 || n_block_rows < 0 ||
+        nblocks < 0 || sizemax < 0 || lut_len < 2 * n_block_rows || !valid_dtype(dtype))
+        return 1;
+    const int64_t bb = block * block;
+    if ((Z > 1 && (y_zstride < nblocks * bb || dy_zstride < nblocks * bb ||
+                   dx_zstride < nblocks * bb)))
+        return 1;
+    const int64_t count = block_rows ? n_listed : n_block_rows;
+    *bad = 0;
+    for (int64_t q = 0; q < count; ++q) {
+        const int64_t rbm = block_rows ? block_rows[q] : q;
+        if (rbm < 0 || rbm >= n_block_rows)
+            return 1;
+        const int64_t size = lut[2 * rbm];
+        const int64_t offset = lut[2 * rbm + 1];
+        int ok = size >= 0 && size <= sizemax;
+        if (ok && size > 0)
+            ok = offset >= 0 && offset + 4 * (size - 1) < lut_len;
+        for (int64_t rbn = 0; ok && rbn < size; ++rbn) {
+            const int64_t blockid = bsr_block_id(lut, offset, rbn);
+            ok = blockid >= 0 && blockid < nblocks;
+        }
+        if (!ok) {
+            ++*bad;
+            continue;
+        }
+        for (int64_t z = 0; z < Z; ++z) {
+            for (int64_t rxm = 0; rxm < block; ++rxm) {
+                /* s = sum of y * dy over the row's stored elements */
+                csum_t s = {0.0, 0.0};
+                for (int64_t rbn = 0; rbn < size; ++rbn) {
+                    const int64_t blockid = bsr_block_id(lut, offset, rbn);
+                    for (int64_t rxn = 0; rxn < block; ++rxn) {
+                        const int64_t e = bsr_index(blockid, rxm, rxn, block);
+                        csum_add(&s, load_elem(y, dtype, z * y_zstride + e) *
+                                         load_elem(dy, dtype, z * dy_zstride + e));
+                    }
+                }
+                const double S = csum_value(&s);
+                /* dx = y * (dy - s) * scale over the same elements */
+                for (int64_t rbn = 0; rbn < size; ++rbn) {
+                    const int64_t blockid = bsr_block_id(lut, offset, rbn);
+                    for (int64_t rxn = 0; rxn < block; ++rxn) {
+                        const int64_t e = bsr_index(blockid, rxm, rxn, block);
+                        dx[z * dx_zstride + e] = load_elem(y, dtype, z * y_zstride + e) *
+                                                 (load_elem(dy, dtype, z * dy_zstride + e) - S) *
+                                                 scale;
+                    }
+                }
+            }
+        }
+    }
+    return 0;
 }

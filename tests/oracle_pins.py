@@ -420,10 +420,147 @@ def pin_reduction_invariants(o):
     assert np.array_equal(l_sel, l_sum[sel])
 
 
+# ---------------------------------------------------------------------------
+# block-sparse softmax backward (look-up table addressing, scale)
+
+def pin_golden_bsr(o):
+    g, cases = {}, []
+    for key, rest in _golden_lines("softmax_bwd_bsr_worked_example.txt"):
+        if key == "case":
+            sizemax, scale, dx, bad = rest.split("|")
+            cases.append((int(sizemax), _expr(scale), _vec(dx), int(bad)))
+        else:
+            g[key] = rest
+    block, nblocks, nbr = int(g["block"]), int(g["nblocks"]), int(g["n_block_rows"])
+    lut = np.array([int(v) for v in g["lut"].split()], dtype=np.int32)
+    y, dy = _vec(g["y"]), _vec(g["dy"])
+    for sizemax, scale, want, want_bad in cases:
+        for arr in (lambda v: np.array([v], dtype=np.float32), lambda v: _bf16([v])):
+            got, bad = o.softmax_bwd_bsr(arr(y), arr(dy), lut, nbr, nblocks, block, sizemax,
+                                         scale)
+            assert bad == want_bad, f"golden bsr: bad {bad}, want {want_bad}"
+            _close(got[0], want, 0, 1e-15, f"golden bsr sizemax={sizemax}")
+
+
+def _bsr_host(t):
+    return workloads_bits(t) if t.dtype == torch.bfloat16 else t.numpy()
+
+
+def _bsr_to_dense(vals, lay, block):
+    """[Z, nblocks * block^2] values -> [Z, H, S, S] float64, zero where no block is
+    stored.  Blocks are numbered in the layout's (head, row, column) order."""
+    Z = vals.shape[0]
+    H, nb, _ = lay.shape
+    v = vals[:, :int(lay.sum()) * block * block].reshape(Z, -1, block, block)
+    dense = np.zeros((Z, H, nb * block, nb * block))
+    for b, (h, r, c) in enumerate(zip(*np.nonzero(lay))):
+        dense[:, h, r * block:(r + 1) * block, c * block:(c + 1) * block] = v[:, b]
+    return dense
+
+
+def _dense_to_bsr(dense, lay, block):
+    out = []
+    for h, r, c in zip(*np.nonzero(lay)):
+        out.append(dense[:, h, r * block:(r + 1) * block, c * block:(c + 1) * block])
+    return np.stack(out, axis=1).reshape(dense.shape[0], -1)
+
+
+def pin_torch_bsr_softmax_bwd(o):
+    """On the dense matrix with zeros where no block is stored, the row-wise
+    softmax backward (torch float64) gives the block-sparse result on the stored
+    blocks: a zero y contributes nothing to sum(y * dy)."""
+    for dtype, block, seed in ((torch.float32, 4, 11), (torch.bfloat16, 8, 11),
+                               (torch.float16, 2, 11)):
+        w = workloads.BsrWorkload("pin", 2, 2, 4 * block, block, dtype, "random", 0.4, seed,
+                                  shuffle=True, diagonal=False)
+        lay = workloads.make_bsr_layout(w)
+        assert (lay.sum(axis=2) == 0).any() and (lay.sum(axis=2) > 1).any()
+        y, dy, lut, meta = workloads.make_bsr_inputs(w)
+        dy_padded = torch.cat([dy, torch.full((w.Z, 8), 7.0, dtype=dtype)], dim=1)
+        scale = 0.75
+        got, bad = o.softmax_bwd_bsr(_bsr_host(y), _bsr_host(dy_padded), lut.numpy(),
+                                     meta["n_block_rows"], meta["nblocks"], block,
+                                     meta["sizemax"], scale)
+        assert bad == 0
+        y64 = y.to(torch.float64).numpy()
+        dy64 = dy.to(torch.float64).numpy()
+        yd = torch.from_numpy(_bsr_to_dense(y64, lay, block))
+        dyd = torch.from_numpy(_bsr_to_dense(dy64, lay, block))
+        ref = _dense_to_bsr(torch._softmax_backward_data(dyd, yd, -1, torch.float64).numpy(),
+                            lay, block) * scale
+        cancel = np.abs(y64) * _dense_to_bsr(
+            np.broadcast_to((yd * dyd).abs().sum(-1, keepdim=True).numpy(), yd.shape), lay,
+            block)
+        tol = 1e-12 * (np.abs(ref) + cancel) + 1e-300
+        assert np.all(np.abs(got - ref) <= tol), f"torch bsr softmax bwd {dtype}"
+
+
+def pin_bsr_table_invariants(o):
+    """The result does not depend on the order of a block-row's entries or on
+    how the blocks are numbered; a padded batch stride changes nothing; a table
+    that is wrong for a block-row leaves exactly that block-row's blocks as dy."""
+    w = workloads.BsrWorkload("pin", 3, 2, 64, 8, torch.float32, "random", 0.3, 21)
+    lay = workloads.make_bsr_layout(w)
+    y, dy, lut, meta = workloads.make_bsr_inputs(w)
+    nbr, nblocks, sizemax = meta["n_block_rows"], meta["nblocks"], meta["sizemax"]
+    hy, hdy = y.numpy(), dy.numpy()
+    base, bad = o.softmax_bwd_bsr(hy, hdy, lut.numpy(), nbr, nblocks, 8, sizemax, 1.5)
+    assert bad == 0
+    # entry order
+    lut2 = workloads.make_bsr_lut(lay, 99)[0]
+    got, _ = o.softmax_bwd_bsr(hy, hdy, lut2, nbr, nblocks, 8, sizemax, 1.5)
+    _close(got, base, 1e-14, 1e-300, "bsr entry order")
+    # block numbering: block b is stored at perm[b]
+    perm = np.random.default_rng(5).permutation(nblocks)
+    def move(a):
+        out = np.empty_like(a).reshape(a.shape[0], nblocks, 64)
+        out[:, perm] = a.reshape(a.shape[0], nblocks, 64)
+        return out.reshape(a.shape)
+    lut3 = lut.numpy().copy()
+    lut3[2 * nbr::4] = perm[lut3[2 * nbr::4]]
+    got, _ = o.softmax_bwd_bsr(move(hy), move(hdy), lut3, nbr, nblocks, 8, sizemax, 1.5)
+    _close(got, move(base), 1e-14, 1e-300, "bsr block numbering")
+    # padded batch stride
+    pad = lambda a: np.concatenate([a, np.full((a.shape[0], 40), 7.0, a.dtype)], axis=1)
+    got, _ = o.softmax_bwd_bsr(pad(hy), pad(hdy), lut.numpy(), nbr, nblocks, 8, sizemax, 1.5)
+    _close(got, base, 0, 1e-300, "bsr batch stride")
+    # wrong tables: one block-row each
+    sizes = lut.numpy()[0:2 * nbr:2]
+    rows = [r for r in range(nbr) if sizes[r] >= 2][:4]
+    assert len(rows) == 4
+    for how, r in zip(("size", "id_high", "id_negative", "offset"), rows):
+        bad_lut = lut.numpy().copy()
+        off = bad_lut[2 * r + 1]
+        if how == "size":
+            got, bad = o.softmax_bwd_bsr(hy, hdy, bad_lut, nbr, nblocks, 8, int(sizes[r]) - 1,
+                                         1.5)
+            wrong = {r2 for r2 in range(nbr) if sizes[r2] > sizes[r] - 1}
+        else:
+            if how == "id_high":
+                bad_lut[off + 4] = nblocks
+            elif how == "id_negative":
+                bad_lut[off] = -1
+            else:
+                bad_lut[2 * r + 1] = bad_lut.size - 4 * int(sizes[r]) + 4
+            got, bad = o.softmax_bwd_bsr(hy, hdy, bad_lut, nbr, nblocks, 8, sizemax, 1.5)
+            wrong = {r}
+        assert bad == len(wrong), f"bsr bad table ({how}): {bad} bad block-rows"
+        mine = np.zeros(nblocks, dtype=bool)
+        for r2 in wrong:
+            ids = lut.numpy()[lut.numpy()[2 * r2 + 1]::4][:sizes[r2]]
+            mine[ids] = True
+        g3 = got.reshape(w.Z, nblocks, 64)
+        assert np.array_equal(g3[:, mine], hdy.reshape(w.Z, nblocks, 64)[:, mine].astype(
+            np.float64)), f"bsr bad table ({how}): rows were written"
+        _close(g3[:, ~mine], base.reshape(w.Z, nblocks, 64)[:, ~mine], 0, 1e-300,
+                f"bsr bad table ({how}): other rows")
+
+
 ALL_PINS = [
     pin_golden_ce, pin_golden_softmax, pin_uniform_closed_form, pin_softmax_uniform,
     pin_ce_invariants, pin_neginf_columns, pin_v1_and_degenerate, pin_softmax_invariants,
     pin_bf16_decoding, pin_row_stride, pin_torch_cross_entropy, pin_torch_softmax,
     pin_finite_difference_ce, pin_finite_difference_softmax_bwd,
     pin_decoding_exhaustive, pin_torch_reductions, pin_reduction_invariants,
+    pin_golden_bsr, pin_torch_bsr_softmax_bwd, pin_bsr_table_invariants,
 ]

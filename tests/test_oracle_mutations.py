@@ -54,6 +54,23 @@ MUTANTS = [
      "uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 15;"),
     ("row_stride_ignored", "(size_t)r * (size_t)j->a_stride * es;",
      "(size_t)r * (size_t)j->ncols * es;"),
+    ("bsr_block_transposed", "return blockid * block * block + rxm * block + rxn;",
+     "return blockid * block * block + rxn * block + rxm;"),
+    ("bsr_entry_stride_2", "return lut[offset + 4 * rbn];", "return lut[offset + 2 * rbn];"),
+    ("bsr_scale_ignored", "(load_elem(dy, dtype, z * dy_zstride + e) - S) *\n"
+     "                                                 scale;",
+     "(load_elem(dy, dtype, z * dy_zstride + e) - S);"),
+    ("bsr_sum_skips_last_block",
+     "csum_t s = {0.0, 0.0};\n                for (int64_t rbn = 0; rbn < size; ++rbn) {",
+     "csum_t s = {0.0, 0.0};\n                for (int64_t rbn = 0; rbn < size - 1; ++rbn) {"),
+    ("bsr_dy_batch_stride_of_y", "load_elem(dy, dtype, z * dy_zstride + e));",
+     "load_elem(dy, dtype, z * y_zstride + e));"),
+    ("bsr_last_row_of_block_skipped", "for (int64_t rxm = 0; rxm < block; ++rxm) {",
+     "for (int64_t rxm = 0; rxm < block - 1; ++rxm) {"),
+    ("bsr_sizemax_not_checked", "int ok = size >= 0 && size <= sizemax;", "int ok = size >= 0;"),
+    ("bsr_sum_of_y", "csum_add(&s, load_elem(y, dtype, z * y_zstride + e) *\n"
+     "                                         load_elem(dy, dtype, z * dy_zstride + e));",
+     "csum_add(&s, load_elem(y, dtype, z * y_zstride + e));"),
 ]
 
 

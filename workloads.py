@@ -23,9 +23,24 @@ Workloads (shapes, value distributions, ignore fractions and seeds):
 "x% rows ignored" means exactly round(x% * M) rows, picked by a seeded
 permutation, get target = ignore_index (-100); every other target is uniform
 in [0, V).
+
+Block-sparse softmax backward workloads (the attention-style layouts the
+block-sparse kernel's look-up table describes: Z batch items, H heads, an
+S x S matrix per head cut into block x block tiles):
+
+  bsr_f32_causal_2x16x4096_b32   fp32, Z=2, H=16, S=4096, block 32, causal layout
+                                 (block-row i holds blocks 0..i), seed 5
+  bsr_bf16_random_4x8x8192_b64   bf16, Z=4, H=8, S=8192, block 64, the diagonal
+                                 block plus each other block with probability 0.1,
+                                 entries of a block-row in random order, seed 6
+
+y is Exp(1) divided by the number of stored elements of its row (so rows sum
+to about 1, like a softmax output) and dy ~ N(0, 1).
 """
 from dataclasses import dataclass, replace
 from typing import Optional
+
+import numpy as np
 
 import torch
 
@@ -129,3 +144,102 @@ def make_softmax_inputs(M: int, N: int, dtype=torch.float32, seed: int = SOFTMAX
     y = e / e.sum(dim=1, keepdim=True)
     return (_place(x.to(dtype), x_stride, pad_fill), _place(y.to(dtype), None, pad_fill),
             _place(dy.to(dtype), dy_stride, pad_fill))
+
+
+# ---------------------------------------------------------------------------
+# block-sparse layouts and their look-up table
+
+@dataclass(frozen=True)
+class BsrWorkload:
+    name: str
+    Z: int            # batch items
+    H: int            # heads
+    S: int            # rows (and columns) of each head's matrix
+    block: int
+    dtype: torch.dtype
+    layout: str       # "causal" or "random"
+    density: float    # "random": probability of each off-diagonal block
+    seed: int
+    shuffle: bool = False   # entries of each block-row in a seeded random order
+    diagonal: bool = True   # "random": always keep the diagonal block
+
+    def with_sizes(self, **kw) -> "BsrWorkload":
+        return replace(self, **kw)
+
+
+BSR_WORKLOADS = {
+    w.name: w for w in [
+        BsrWorkload("bsr_f32_causal_2x16x4096_b32", 2, 16, 4096, 32, torch.float32, "causal",
+                    0.0, 5),
+        BsrWorkload("bsr_bf16_random_4x8x8192_b64", 4, 8, 8192, 64, torch.bfloat16, "random",
+                    0.1, 6, shuffle=True),
+    ]
+}
+
+
+def make_bsr_layout(w: BsrWorkload) -> np.ndarray:
+    """Boolean [H, S/block, S/block]: which blocks are stored."""
+    nb = w.S // w.block
+    assert nb * w.block == w.S
+    if w.layout == "causal":
+        one = np.tril(np.ones((nb, nb), dtype=bool))
+        return np.broadcast_to(one, (w.H, nb, nb)).copy()
+    assert w.layout == "random"
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    lay = rng.random((w.H, nb, nb)) < w.density
+    if w.diagonal:
+        lay[:, np.arange(nb), np.arange(nb)] = True
+    return lay
+
+
+def make_bsr_lut(layout: np.ndarray, shuffle_seed: Optional[int] = None):
+    """(lut int32, n_block_rows, nblocks, sizemax, block_row_of_block int64).
+
+    Blocks are numbered in (head, block-row, block-column) order.  The table
+    starts with one (size, offset) pair per block-row (head-major); each
+    stored block then has a 4-int entry (block id, head, block-row,
+    block-column) at offset + 4 * k.  With a seed, the entries of each
+    block-row are put in a random order.
+    """
+    H, nb, _ = layout.shape
+    nbr = H * nb
+    h, r, c = np.nonzero(layout)                 # (h, r, c) in row-major order
+    nblocks = h.size
+    sizes = layout.reshape(nbr, nb).sum(axis=1).astype(np.int64)
+    starts = np.zeros(nbr, dtype=np.int64)
+    np.cumsum(sizes[:-1], out=starts[1:])
+    entries = np.stack([np.arange(nblocks), h, r, c], axis=1).astype(np.int64)
+    if shuffle_seed is not None and nblocks:
+        rng = np.random.Generator(np.random.PCG64(shuffle_seed))
+        row_of = h * nb + r
+        order = np.lexsort((rng.random(nblocks), row_of))
+        entries = entries[order]
+    lut = np.empty(2 * nbr + 4 * nblocks, dtype=np.int64)
+    lut[0:2 * nbr:2] = sizes
+    lut[1:2 * nbr:2] = 2 * nbr + 4 * starts
+    lut[2 * nbr:] = entries.reshape(-1)
+    sizemax = int(sizes.max()) if nbr else 0
+    return lut.astype(np.int32), nbr, nblocks, sizemax, (h * nb + r).astype(np.int64)
+
+
+def make_bsr_inputs(w: BsrWorkload, device="cpu", zpad: int = 0):
+    """(y, dy, lut, meta): y and dy are [Z, nblocks * block^2 + zpad] tensors of
+    w.dtype (block b of item z at b * block^2), lut an int32 tensor, meta a dict
+    with n_block_rows, nblocks, block, sizemax.  Draw order: the layout and the
+    entry order on the CPU (numpy PCG64), then y ~ Exp(1) and dy ~ N(0, 1) with
+    torch's generator on ``device``; y is divided by its row's element count."""
+    lay = make_bsr_layout(w)
+    lut, nbr, nblocks, sizemax, brow = make_bsr_lut(lay, w.seed + 1 if w.shuffle else None)
+    bb = w.block * w.block
+    g = _gen(device, w.seed)
+    L = nblocks * bb
+    y = torch.empty((w.Z, L), device=device, dtype=torch.float32).exponential_(generator=g)
+    dy = torch.randn((w.Z, L), generator=g, device=device, dtype=torch.float32)
+    sizes = torch.from_numpy(lut[0:2 * nbr:2].astype(np.int64)).to(device)
+    count = (sizes[torch.from_numpy(brow).to(device)] * w.block).to(torch.float32)
+    y = (y.view(w.Z, nblocks, bb) / count.view(1, nblocks, 1)).view(w.Z, L)
+    if zpad:
+        y = torch.cat([y, torch.full((w.Z, zpad), 7.0, device=device)], dim=1)
+        dy = torch.cat([dy, torch.full((w.Z, zpad), 7.0, device=device)], dim=1)
+    meta = dict(n_block_rows=nbr, nblocks=nblocks, block=w.block, sizemax=sizemax)
+    return (y.to(w.dtype), dy.to(w.dtype), torch.from_numpy(lut).to(device), meta)
