@@ -350,6 +350,49 @@ def time_softmax(steps, warmup, ws, flush, N=16384):
     return times["fwd"], times["bwd"], M, N
 
 
+def bsr_algorithmic_bytes(meta, Z, es, lut_len) -> int:
+    """Two reads (y, dy) and one write (dx) of every stored element, plus the table."""
+    return 3 * Z * meta["nblocks"] * meta["block"] ** 2 * es + 4 * lut_len
+
+
+def time_bsr(steps, warmup, ws, flush, peak):
+    """Block-sparse softmax backward on each block-sparse workload (dx out of
+    place, so every step sees the same inputs): kernel time from the library's
+    events, L2 flushed before each call."""
+    import cross_entropy_loss_ce_gb300 as gbce
+    out = []
+    for w in workloads.BSR_WORKLOADS.values():
+        y, dy, lut, meta = workloads.make_bsr_inputs(w, device="cuda")
+        dx = torch.empty_like(dy)
+        call = lambda: gbce.softmax_bwd_bsr(y, dy, lut, meta["n_block_rows"], meta["nblocks"],
+                                            meta["block"], meta["sizemax"], 1.0, dx)
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        gbce.timing_read()
+        gbce.timing_enable(True)
+        for _ in range(steps):
+            flush_l2(flush)
+            barrier_sync(ws)
+            call()
+        barrier_sync(ws)
+        ms, n = gbce.timing_read()
+        gbce.timing_enable(False)
+        if gbce.last_error() != gbce.OK:
+            raise RuntimeError("device error flag raised")
+        ms = max_over_ranks(ms / max(n, 1), ws)
+        b = bsr_algorithmic_bytes(meta, w.Z, esize(w.dtype), lut.numel())
+        rows = w.Z * meta["n_block_rows"] * meta["block"]
+        kernel, R = gbce.bsr_plan(meta["block"], meta["sizemax"], w.dtype)
+        out.append({"workload": w.name, "kernel": kernel, "rows_per_cta": R,
+                    "timing": "kernel, CUDA events", "kernel_ms": ms,
+                    "rows_per_s": rows / (ms / 1e3), "algorithmic_bytes": b,
+                    "gbs": b / (ms / 1e3) / 1e9, "frac": b / (ms / 1e3) / 1e9 / peak})
+        del y, dy, dx
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_gbce(args, ws, rank, local):
     import cross_entropy_loss_ce_gb300 as gbce
     gbce.load_library()
@@ -402,6 +445,9 @@ def run_gbce(args, ws, rank, local):
             "fwd_gbs": fwd_b / (fwd_ms / 1e3) / 1e9, "bwd_gbs": bwd_b / (bwd_ms / 1e3) / 1e9,
             "fwd_frac": fwd_b / (fwd_ms / 1e3) / 1e9 / peak,
             "bwd_frac": bwd_b / (bwd_ms / 1e3) / 1e9 / peak}
+
+    if not args.no_softmax:
+        line["softmax_bsr"] = time_bsr(max(args.steps // 2, 5), args.warmup, ws, flush, peak)
 
     if not args.no_e2e:
         x_pinned = xd0.cpu().pin_memory()
@@ -478,6 +524,12 @@ def run_table(args, local):
                               "rows_per_s": M / (ms / 1e3), "alg_gbs": b / (ms / 1e3) / 1e9,
                               "frac_of_measured_peak": b / (ms / 1e3) / 1e9 / peak}), flush=True)
 
+    for r in time_bsr(steps, args.warmup, 1, flush, peak):
+        print(json.dumps({"table": r["workload"], "kernel_us": 1e3 * r["kernel_ms"],
+                          "rows_per_s": r["rows_per_s"], "alg_gbs": r["gbs"],
+                          "frac_of_measured_peak": r["frac"], "kernel": r["kernel"],
+                          "rows_per_cta": r["rows_per_cta"]}), flush=True)
+
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
@@ -491,7 +543,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=16384)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-softmax", action="store_true")
+    ap.add_argument("--no-softmax", action="store_true",
+                    help="skip the row softmax and block-sparse softmax backward timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--table", action="store_true",
                     help="print the kernel time of every workload instead of the benchmark line")

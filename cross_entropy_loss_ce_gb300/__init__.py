@@ -19,7 +19,7 @@ DTYPES = {torch.float32: GBCE_F32, torch.bfloat16: GBCE_BF16, torch.float16: GBC
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 OK, ERR_NULL, ERR_SIZE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA, ERR_BAD_TARGET, ERR_TIMEOUT, \
-    ERR_NO_DEVICE, ERR_REDUCTION = range(10)
+    ERR_NO_DEVICE, ERR_REDUCTION, ERR_BAD_TABLE = range(11)
 
 _lib = None
 
@@ -50,10 +50,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gbce_status_string.argtypes = [ci]
         lib.gbce_status_string.restype = ctypes.c_char_p
         lib.gbce_timing_enable.argtypes = [ci]
+        lib.softmax_bwd_bsr.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, i64, i64,
+                                        ctypes.c_float, ci, p]
+        lib.gbce_bsr_plan.argtypes = [i64, i64, ci, ci, ctypes.POINTER(ci)]
+        lib.gbce_bsr_plan.restype = ctypes.c_char_p
         lib.gbce_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
                                          ctypes.POINTER(ctypes.c_int64)]
         for f in ("ce_fwd_bwd", "softmax_fwd", "softmax_bwd", "gbce_last_error",
-                  "gbce_timing_enable", "gbce_timing_read", "ce_fwd_bwd_ex", "scale_rows"):
+                  "gbce_timing_enable", "gbce_timing_read", "ce_fwd_bwd_ex", "scale_rows",
+                  "softmax_bwd_bsr"):
             getattr(lib, f).restype = ci
         _lib = lib
     return _lib
@@ -239,6 +244,46 @@ def softmax_bwd(y: torch.Tensor, dy: torch.Tensor, dx: torch.Tensor = None,
                                     _stream_handle(stream))
     _check(rc, "softmax_bwd")
     return dx
+
+
+def softmax_bwd_bsr(y: torch.Tensor, dy: torch.Tensor, lut: torch.Tensor, n_block_rows: int,
+                    nblocks: int, block: int, sizemax: int, scale: float = 1.0,
+                    dx: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Block-sparse softmax backward, dx = y * (dy - sum(y * dy)) * scale per row.
+
+    ``y``, ``dy`` and ``dx`` are [Z, zstride] CUDA tensors (unit inner stride)
+    whose first nblocks * block^2 elements per batch item hold the blocks;
+    ``lut`` is the int32 look-up table (a contiguous CUDA tensor).  ``dx``
+    defaults to ``dy`` (in place, as the page's kernel stores); only the
+    positions the table names are written.
+    """
+    if dx is None:
+        dx = dy
+    yp, ys, Z, Ly = _matrix(y, "y")
+    dp, ds, Zd, Ld = _matrix(dy, "dy")
+    xp, xs, Zx, Lx = _matrix(dx, "dx")
+    if Zd != Z or Zx != Z or not (y.dtype == dy.dtype == dx.dtype):
+        raise ValueError("y, dy and dx must share the batch size and dtype")
+    if min(Ly, Ld, Lx) < nblocks * block * block:
+        raise ValueError("y, dy and dx must hold nblocks * block^2 elements per batch item")
+    if lut.dtype != torch.int32 or lut.dim() != 1 or not lut.is_cuda or not lut.is_contiguous():
+        raise ValueError("lut must be a contiguous 1-D int32 CUDA tensor")
+    rc = load_library().softmax_bwd_bsr(yp, ys, dp, ds, xp, xs, lut.data_ptr(), lut.numel(),
+                                        n_block_rows, nblocks, block, sizemax, Z, float(scale),
+                                        DTYPES[y.dtype], _stream_handle(stream))
+    _check(rc, "softmax_bwd_bsr")
+    return dx
+
+
+def bsr_plan(block: int, sizemax: int, dtype: torch.dtype, aligned: bool = True):
+    """(kernel name, rows per CTA) softmax_bwd_bsr uses for this block size,
+    longest block-row and dtype."""
+    r = ctypes.c_int(0)
+    name = load_library().gbce_bsr_plan(block, sizemax, DTYPES[dtype], 1 if aligned else 0,
+                                        ctypes.byref(r))
+    if name is None:
+        raise ValueError("invalid block-sparse plan query")
+    return name.decode(), r.value
 
 
 def plan(op: str, cols: int, dtype: torch.dtype, same_phase: bool = True):

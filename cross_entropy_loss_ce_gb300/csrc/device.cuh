@@ -14,7 +14,7 @@ constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = exp2(x * log
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bulk copy that takes 2 s has failed
 
 // Sticky per-device error flags (read and cleared by gbce_last_error()).
-enum : unsigned { kFlagBadTarget = 1u, kFlagTimeout = 2u };
+enum : unsigned { kFlagBadTarget = 1u, kFlagTimeout = 2u, kFlagBadTable = 4u };
 
 // ---------------------------------------------------------------------------
 // small PTX wrappers

@@ -11,6 +11,7 @@
 
 #include "../../include/gbce.h"
 #include "row_kernels.cuh"
+#include "bsr_kernels.cuh"
 
 namespace gbce {
 namespace {
@@ -26,6 +27,9 @@ constexpr int kRingWarps = 16;                // consumer warps of the ring kern
 constexpr int kRingVpt1 = 4;                  // vectors per consumer thread and slot, one operand
 constexpr int kRingVpt2 = 2;                  // the same, two operands (softmax backward)
 constexpr int64_t kL2Budget = 56ll << 20;     // bytes of rows between their two reads, all SMs
+constexpr int64_t kBsrTarget = 48 * 1024;     // block-sparse: staged bytes per CTA aimed at
+constexpr int kBsrThreads = 256;              // block-sparse kernels' CTA size
+constexpr int kBsrMaxRows = 64;               // rows per staged CTA (<= kBsrThreads / 4)
 
 size_t elem_size(int dtype) { return dtype == GBCE_F32 ? 4 : 2; }
 
@@ -171,7 +175,7 @@ KernelFn pick(int dtype, const Plan &p)
 // Per-device one-time function attributes (large dynamic shared memory,
 // cluster sizes above the portable 8).
 struct FnConfig {
-    KernelFn fn;
+    const void *fn;
     int device;
 };
 struct GridCache {
@@ -184,23 +188,26 @@ std::vector<GridCache> g_grid;
 std::mutex g_cfg_mu;
 std::vector<FnConfig> g_cfg;
 
-cudaError_t configure(KernelFn fn, int device)
+cudaError_t configure(const void *fn, int device)
 {
     std::lock_guard<std::mutex> lk(g_cfg_mu);
     for (const FnConfig &c : g_cfg)
         if (c.fn == fn && c.device == device)
             return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSliceMax));
     if (e != cudaSuccess)
         return e;
-    e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess)
         return e;
     g_cfg.push_back({fn, device});
     return cudaSuccess;
+}
+
+cudaError_t configure(KernelFn fn, int device)
+{
+    return configure(reinterpret_cast<const void *>(fn), device);
 }
 
 // ---------------------------------------------------------------------------
@@ -502,6 +509,97 @@ int ce_call(void *logits, int64_t stride, const int64_t *targets, float *loss, f
     return map_error(e);
 }
 
+// ---------------------------------------------------------------------------
+// block-sparse softmax backward
+
+struct BsrPlan {
+    bool staged;     // bsr_bwd_staged_kernel, else bsr_bwd_unstaged_kernel
+    bool vec;        // 16-byte accesses, else one element at a time
+    int log2_R;      // staged: rows per CTA = 2^log2_R
+    int ids_bytes;   // staged: shared bytes for the block ids
+    int64_t smem;    // staged: dynamic shared memory per CTA
+};
+
+int log2_exact(int64_t v)
+{
+    int l = 0;
+    while ((int64_t{1} << l) < v)
+        ++l;
+    return l;
+}
+
+// Rows of sizemax * block elements: stage R rows per CTA (both operands and
+// the block ids in shared memory), R the largest power of two <= min(block,
+// kBsrMaxRows) within kBsrTarget bytes (one row at least, up to kSliceMax);
+// rows beyond kSliceMax go to the unstaged kernel.  `aligned`: the operands'
+// bases and batch strides allow 16-byte accesses.
+BsrPlan make_bsr_plan(int64_t block, int64_t sizemax, size_t es, bool aligned)
+{
+    BsrPlan p{};
+    const int log2_block = log2_exact(block);
+    p.vec = aligned && block * static_cast<int64_t>(es) >= 16;
+    p.ids_bytes = static_cast<int>((sizemax * 4 + 15) / 16 * 16);
+    const int64_t row2 = sizemax * block * static_cast<int64_t>(es) * 2;
+    if (p.ids_bytes + row2 > kSliceMax) {
+        p.staged = false;
+        return p;
+    }
+    p.staged = true;
+    const int64_t budget = kBsrTarget > p.ids_bytes + row2 ? kBsrTarget : p.ids_bytes + row2;
+    int l = 0;
+    while (l < log2_block && (1 << (l + 1)) <= kBsrMaxRows && p.ids_bytes + (row2 << (l + 1)) <= budget)
+        ++l;
+    p.log2_R = l;
+    p.smem = p.ids_bytes + (row2 << l);
+    return p;
+}
+
+using BsrFn = void (*)(const BsrArgs);
+
+template <typename T>
+BsrFn pick_bsr_t(const BsrPlan &p)
+{
+    constexpr int V = 16 / sizeof(T);
+    if (p.staged)
+        return p.vec ? bsr_bwd_staged_kernel<T, V, kBsrThreads>
+                     : bsr_bwd_staged_kernel<T, 1, kBsrThreads>;
+    return p.vec ? bsr_bwd_unstaged_kernel<T, V, kBsrThreads>
+                 : bsr_bwd_unstaged_kernel<T, 1, kBsrThreads>;
+}
+
+BsrFn pick_bsr(int dtype, const BsrPlan &p)
+{
+    switch (dtype) {
+    case GBCE_F32: return pick_bsr_t<float>(p);
+    case GBCE_F16: return pick_bsr_t<__half>(p);
+    default: return pick_bsr_t<__nv_bfloat16>(p);
+    }
+}
+
+bool valid_dtype(int dtype) { return dtype == GBCE_F32 || dtype == GBCE_BF16 || dtype == GBCE_F16; }
+
+// Shape checks of softmax_bwd_bsr that need no pointer.
+int check_bsr_shape(int64_t y_zstride, int64_t dy_zstride, int64_t dx_zstride, int64_t lut_len,
+                    int64_t n_block_rows, int64_t nblocks, int64_t block, int64_t sizemax,
+                    int64_t Z, int dtype)
+{
+    if (!valid_dtype(dtype))
+        return GBCE_ERR_DTYPE;
+    if (block < 1 || block > 1024 || (block & (block - 1)) || Z < 0 || n_block_rows < 0 ||
+        nblocks < 0 || sizemax < 0 || sizemax > INT32_MAX / block || lut_len < 2 * n_block_rows)
+        return GBCE_ERR_SIZE;
+    const int64_t bb = block * block;
+    if (nblocks > kMaxStride / bb)
+        return GBCE_ERR_SIZE;
+    if (Z > 1) {
+        const int64_t need = nblocks * bb;
+        for (int64_t st : {y_zstride, dy_zstride, dx_zstride})
+            if (st < need || st > kMaxStride)
+                return GBCE_ERR_SIZE;
+    }
+    return GBCE_OK;
+}
+
 }  // namespace
 }  // namespace gbce
 
@@ -671,6 +769,8 @@ extern "C" int gbce_last_error(gbce_stream_t stream_)
         return map_error(e);
     if (flags & kFlagBadTarget)
         return GBCE_ERR_BAD_TARGET;
+    if (flags & kFlagBadTable)
+        return GBCE_ERR_BAD_TABLE;
     if (flags & kFlagTimeout)
         return GBCE_ERR_TIMEOUT;
     return GBCE_OK;
@@ -689,6 +789,7 @@ extern "C" const char *gbce_status_string(int status)
     case GBCE_ERR_TIMEOUT: return "a bounded wait for an asynchronous copy gave up";
     case GBCE_ERR_NO_DEVICE: return "no usable CUDA device";
     case GBCE_ERR_REDUCTION: return "reduction is not a gbce_reduction";
+    case GBCE_ERR_BAD_TABLE: return "a block-sparse look-up table entry is malformed";
     default: return "unknown status";
     }
 }
@@ -801,4 +902,79 @@ extern "C" int ce_fwd_bwd_noalloc(void *logits, int64_t stride, const int64_t *t
     e = launch_ce(logits, stride, targets, loss, nullptr, nullptr, M, V, ignore_index, dtype,
                   GBCE_MEAN, scratch, stream);
     return map_error(e);
+}
+
+extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
+                               int64_t dy_zstride, void *dx, int64_t dx_zstride,
+                               const int32_t *lut, int64_t lut_len, int64_t n_block_rows,
+                               int64_t nblocks, int64_t block, int64_t sizemax, int64_t Z,
+                               float scale, int dtype, gbce_stream_t stream_)
+{
+    int st = check_bsr_shape(y_zstride, dy_zstride, dx_zstride, lut_len, n_block_rows, nblocks,
+                             block, sizemax, Z, dtype);
+    if (st)
+        return st;
+    if (Z == 0 || n_block_rows == 0 || sizemax == 0)
+        return GBCE_OK;
+    if (!y || !dy || !dx || !lut)
+        return GBCE_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (!aligned_to(y, es) || !aligned_to(dy, es) || !aligned_to(dx, es) || !aligned_to(lut, 4))
+        return GBCE_ERR_ALIGN;
+    const bool aligned =
+        aligned_to(y, 16) && aligned_to(dy, 16) && aligned_to(dx, 16) &&
+        (Z <= 1 || ((y_zstride * static_cast<int64_t>(es)) % 16 == 0 &&
+                    (dy_zstride * static_cast<int64_t>(es)) % 16 == 0 &&
+                    (dx_zstride * static_cast<int64_t>(es)) % 16 == 0));
+    const BsrPlan p = make_bsr_plan(block, sizemax, es, aligned);
+    const int log2_block = log2_exact(block);
+    const int per_row_block = p.staged ? log2_block - p.log2_R : log2_block;
+    // units = Z * n_block_rows * 2^per_row_block must fit a 1-D grid
+    const int64_t kGridMax = INT32_MAX;
+    if (n_block_rows > (kGridMax >> per_row_block) ||
+        Z > (kGridMax >> per_row_block) / n_block_rows)
+        return GBCE_ERR_SIZE;
+    const int64_t units = (Z * n_block_rows) << per_row_block;
+
+    BsrArgs a{};
+    a.y = y;
+    a.ys = y_zstride;
+    a.dy = dy;
+    a.dys = dy_zstride;
+    a.dx = dx;
+    a.dxs = dx_zstride;
+    a.lut = lut;
+    a.lut_len = lut_len;
+    a.nbr = n_block_rows;
+    a.nblocks = nblocks;
+    a.log2_block = log2_block;
+    a.log2_R = p.log2_R;
+    a.sizemax = static_cast<int>(sizemax);
+    a.ids_bytes = p.ids_bytes;
+    a.scale = scale;
+
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return map_error(e);
+    const BsrFn fn = pick_bsr(dtype, p);
+    if ((e = configure(reinterpret_cast<const void *>(fn), device)) != cudaSuccess)
+        return map_error(e);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    TimedRegion timed(stream);
+    fn<<<static_cast<unsigned>(units), kBsrThreads, p.staged ? p.smem : 0, stream>>>(a);
+    return map_error(cudaGetLastError());
+}
+
+extern "C" const char *gbce_bsr_plan(int64_t block, int64_t sizemax, int dtype, int aligned,
+                                     int *rows_per_cta)
+{
+    if (check_bsr_shape(0, 0, 0, 0, 0, 0, block, sizemax, 0, dtype) != GBCE_OK || sizemax < 1)
+        return nullptr;
+    const BsrPlan p = make_bsr_plan(block, sizemax, elem_size(dtype), aligned != 0);
+    if (rows_per_cta)
+        *rows_per_cta = p.staged ? 1 << p.log2_R : 1;
+    if (p.staged)
+        return p.vec ? "bsr_bwd_staged_kernel" : "bsr_bwd_staged_kernel (element accesses)";
+    return p.vec ? "bsr_bwd_unstaged_kernel" : "bsr_bwd_unstaged_kernel (element accesses)";
 }

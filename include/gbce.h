@@ -62,7 +62,8 @@ enum gbce_status {
     GBCE_ERR_BAD_TARGET = 6,  /* device flag: a target outside [0, V) that is not ignore_index */
     GBCE_ERR_TIMEOUT = 7,     /* device flag: a bounded wait on an asynchronous copy gave up */
     GBCE_ERR_NO_DEVICE = 8,   /* no usable CUDA device */
-    GBCE_ERR_REDUCTION = 9    /* reduction is not a gbce_reduction */
+    GBCE_ERR_REDUCTION = 9,   /* reduction is not a gbce_reduction */
+    GBCE_ERR_BAD_TABLE = 10   /* device flag: a block-sparse look-up table entry is malformed */
 };
 
 /*
@@ -202,6 +203,57 @@ GBCE_API int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int64_
                 int64_t dx_stride, int64_t M, int64_t N, int dtype, gbce_stream_t stream);
 
 /*
+ * softmax_bwd_bsr -- block-sparse softmax backward through a look-up table,
+ * dx = y * (dy - sum(y * dy)) * scale over every row of a block-sparse matrix.
+ *
+ * Defined by: "python sum function examples (triton.language)", _backward
+ * (the block-sparse softmax backward with its look-up table and `scale`).
+ *
+ * Storage: Z batch items; item z of an operand starts at z * <op>_zstride
+ * elements.  Each item holds `nblocks` blocks of block x block elements, block
+ * b at b * block^2, row-major inside the block.
+ *
+ *   lut [lut_len] int32, device memory.  lut[2 rbm] = size and lut[2 rbm + 1] =
+ *     offset for block-row rbm = 0 .. n_block_rows-1; the block-row's blocks are
+ *     lut[offset + 4 k], k = 0 .. size-1 (entries of 4 ints, block id first;
+ *     the other three ints are not read).  Row rxm of block-row rbm (matrix row
+ *     rbm * block + rxm) is the concatenation of row rxm of those blocks.  Each
+ *     block belongs to one block-row; a block listed twice gives unspecified
+ *     values (no memory error).
+ *   y  softmax output, read.   dy upstream gradient, read.
+ *   dx written at every position the table names, nothing else; dx may be dy
+ *     (same zstride), as in the page's in-place store; other overlaps are not
+ *     allowed.
+ *   block     a power of two, 1 .. 1024.
+ *   sizemax   the largest size of any block-row (sizemax * block < 2^31); it
+ *             sets the shared-memory plan, so pass the table's true maximum.
+ *   scale     multiplies the result.
+ * Batch strides are ignored when Z <= 1, else must be >= nblocks * block^2.
+ * Argument errors (GBCE_ERR_DTYPE, _SIZE, _NULL, _ALIGN) are returned before
+ * any launch.  Z, n_block_rows or sizemax of 0: nothing to do, GBCE_OK.  A
+ * block-row whose size is negative or above sizemax, whose entries run past
+ * lut_len, or that names a block outside [0, nblocks) is left unwritten for
+ * every batch item and raises GBCE_ERR_BAD_TABLE in gbce_last_error();
+ * nothing outside the named blocks is read or written.
+ */
+GBCE_API int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy, int64_t dy_zstride,
+                             void *dx, int64_t dx_zstride, const int32_t *lut, int64_t lut_len,
+                             int64_t n_block_rows, int64_t nblocks, int64_t block,
+                             int64_t sizemax, int64_t Z, float scale, int dtype,
+                             gbce_stream_t stream);
+
+/*
+ * gbce_bsr_plan -- the kernel softmax_bwd_bsr uses for `block`, `sizemax` and
+ * `dtype` ("bsr_bwd_staged_kernel": slabs of *rows_per_cta rows of a
+ * block-row staged in shared memory; "bsr_bwd_unstaged_kernel": one row per
+ * CTA, two passes over global memory; " (element accesses)" appended when
+ * `aligned` is 0 or a block row is under 16 bytes).  NULL for invalid
+ * arguments.  For tests and diagnostics; no kernel is launched.
+ */
+GBCE_API const char *gbce_bsr_plan(int64_t block, int64_t sizemax, int dtype, int aligned,
+                                   int *rows_per_cta);
+
+/*
  * gbce_plan -- the row-kernel family a call uses for rows of `cols` elements
  * of `dtype` on the current device: "rows_warp_kernel" (rows of at most 8 KB
  * per operand, one warp per row), "rows_resident_kernel" (at most 64 KB
@@ -217,8 +269,8 @@ GBCE_API const char *gbce_plan(int op, int64_t cols, int dtype, int same_phase, 
 /*
  * gbce_last_error -- synchronise `stream`, then read and clear the current
  * device's sticky error flags.  Returns GBCE_OK, GBCE_ERR_BAD_TARGET,
- * GBCE_ERR_TIMEOUT (when both are set, BAD_TARGET), or GBCE_ERR_CUDA when the
- * synchronisation itself failed.
+ * GBCE_ERR_BAD_TABLE or GBCE_ERR_TIMEOUT (the first of these that is set, in
+ * this order), or GBCE_ERR_CUDA when the synchronisation itself failed.
  */
 GBCE_API int gbce_last_error(gbce_stream_t stream);
 

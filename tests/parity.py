@@ -3,7 +3,9 @@
 fp32 (results computed and stored in fp32):
   gradient / softmax:   |g - o| <= 1e-5 |o| + FLOOR
   softmax backward:     |dx - o| <= 1e-5 (|o| + |y_i| sum_j |y_j dy_j|) + FLOOR
-                        (the second term bounds the cancellation in dy_i - s)
+                        (the second term bounds the cancellation in dy_i - s; for the
+                        block-sparse form it is multiplied by |scale| and the sum runs
+                        over the row's stored elements)
   loss:                 |L - Lo| <= 1e-5 |Lo|
 bf16 (fp32 arithmetic, one round-to-nearest-even store):
   gradient:             |n g - n o| <= 2e-2            (the stated bound, on p - onehot)
@@ -121,3 +123,17 @@ def ulp_distance_16(got: torch.Tensor, ref: np.ndarray, dtype) -> np.ndarray:
         return np.where(v & 0x8000, -mag, mag)
 
     return np.abs(line(a) - line(b))
+
+
+def check_bsr(got: np.ndarray, ref: np.ndarray, y: np.ndarray, row_abs: np.ndarray, scale: float,
+              dtype, what="block-sparse softmax backward"):
+    """got, ref, y (float64) and row_abs = sum over the element's row of |y dy|,
+    all of one shape; the bound of check_softmax_bwd with the cancellation term
+    scaled by |scale|."""
+    cancel = abs(scale) * np.abs(y) * row_abs
+    if dtype == torch.float32:
+        tol = 1e-5 * (np.abs(ref) + cancel) + FLOOR
+    else:
+        rel, floor = rel_floor(dtype)
+        tol = (rel - 1e-5) * np.abs(ref) + 2e-5 * cancel + floor
+    _report(~(np.abs(got - ref) <= tol), got, ref, tol, what)

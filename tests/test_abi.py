@@ -30,6 +30,10 @@ def lib():
     lib.ce_fwd_bwd_ex.argtypes = [p, i64, p, p, p, p, i64, i64, i64, ci, ci, p]
     lib.scale_rows.argtypes = [p, i64, i64, i64, ci, p, ci, p]
     lib.gbce_status_string.restype = ctypes.c_char_p
+    lib.softmax_bwd_bsr.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, i64, i64,
+                                    ctypes.c_float, ci, p]
+    lib.gbce_bsr_plan.argtypes = [i64, i64, ci, ci, ctypes.POINTER(ci)]
+    lib.gbce_bsr_plan.restype = ctypes.c_char_p
     return lib
 
 
@@ -37,7 +41,7 @@ def test_header_declares_the_boundary():
     names = set(declared_functions())
     assert {"ce_fwd_bwd", "softmax_fwd", "softmax_bwd", "gbce_last_error",
             "gbce_status_string", "gbce_timing_enable", "gbce_timing_read", "ce_fwd_bwd_ex",
-            "scale_rows"} <= names
+            "scale_rows", "softmax_bwd_bsr", "gbce_bsr_plan"} <= names
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -52,7 +56,7 @@ def test_only_the_abi_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(10):
+    for code in range(11):
         s = lib.gbce_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.gbce_status_string(99).decode() == "unknown status"
@@ -176,3 +180,50 @@ def test_size_limits(lib):
     assert lib.ce_fwd_bwd(FAKE, 2 ** 47, FAKE, FAKE, 4, 10, -100, 0, None) == 2
     assert lib.ce_fwd_bwd(FAKE, 10, FAKE, FAKE, 2 ** 27, 10, -100, 0, None) == 2
     assert lib.softmax_fwd(FAKE, 2 ** 47, FAKE, 8, 2, 8, 0, None) == 2
+
+
+# softmax_bwd_bsr(y, ys, dy, dys, dx, dxs, lut, lut_len, n_block_rows, nblocks, block,
+#                 sizemax, Z, scale, dtype)
+BSR_OK = (FAKE, 4096, FAKE, 4096, FAKE, 4096, FAKE, 16, 4, 4, 32, 2, 2, 1.0, 0)
+
+
+def _bsr(**kw):
+    names = ["y", "ys", "dy", "dys", "dx", "dxs", "lut", "lut_len", "nbr", "nblocks", "block",
+             "sizemax", "Z", "scale", "dtype"]
+    a = dict(zip(names, BSR_OK))
+    a.update(kw)
+    return tuple(a[n] for n in names)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=3), 3),
+    (dict(block=3), 2), (dict(block=0), 2), (dict(block=2048), 2),
+    (dict(Z=-1), 2), (dict(nbr=-1), 2), (dict(nblocks=-1), 2), (dict(sizemax=-1), 2),
+    (dict(lut_len=7), 2),                                # fewer than 2 ints per block-row
+    (dict(ys=4095), 2), (dict(dxs=100), 2),              # batch stride < nblocks * block^2
+    (dict(sizemax=2**26), 2),                            # sizemax * block >= 2^31
+    (dict(Z=2**40, ys=2**20, dys=2**20, dxs=2**20), 2),  # beyond a 1-D grid
+    (dict(y=None), 1), (dict(dx=None), 1), (dict(lut=None), 1),
+    (dict(y=FAKE + 2), 4), (dict(lut=FAKE + 2), 4), (dict(dtype=1, dy=FAKE + 1), 4),
+    (dict(Z=0, y=None, lut=None), 0), (dict(nbr=0, lut_len=0, lut=None), 0),
+    (dict(sizemax=0, y=None), 0),
+])
+def test_bsr_rejects_bad_arguments(lib, kw, code):
+    assert lib.softmax_bwd_bsr(*_bsr(**kw), None) == code
+
+
+@pytest.mark.parametrize("block,sizemax,dtype,aligned,kernel,rows", [
+    (32, 128, 0, 1, "bsr_bwd_staged_kernel", 1),       # causal S=4096: 32 KB per row
+    (64, 25, 1, 1, "bsr_bwd_staged_kernel", 4),        # random S=8192 bf16
+    (16, 2, 0, 1, "bsr_bwd_staged_kernel", 16),        # tiny rows: as many as the block has
+    (128, 1, 2, 1, "bsr_bwd_staged_kernel", 64),       # capped at 64 rows per CTA
+    (32, 1000, 0, 1, "bsr_bwd_unstaged_kernel", 1),    # 256 KB per row: not staged
+    (2, 3, 0, 1, "bsr_bwd_staged_kernel (element accesses)", 2),   # 8-byte block rows
+    (32, 8, 1, 0, "bsr_bwd_staged_kernel (element accesses)", 32),
+])
+def test_bsr_plan(lib, block, sizemax, dtype, aligned, kernel, rows):
+    r = ctypes.c_int(0)
+    name = lib.gbce_bsr_plan(block, sizemax, dtype, aligned, ctypes.byref(r))
+    assert name.decode() == kernel and r.value == rows
+    assert lib.gbce_bsr_plan(3, 1, 0, 1, None) is None
+    assert lib.gbce_bsr_plan(32, 0, 0, 1, None) is None
