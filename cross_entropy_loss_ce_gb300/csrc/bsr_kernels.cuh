@@ -9,13 +9,15 @@
 // concatenation of row rxm of its blocks.
 //
 // Two kernels, chosen on the host from the longest row (sizemax * block):
-//   bsr_bwd_staged_kernel    one CTA per slab of R rows of one block-row and one
-//                            batch item.  The slab's piece of every listed
-//                            block (R * block contiguous elements per operand)
-//                            is gathered into shared memory with 16-byte
+//   bsr_bwd_staged_kernel    one CTA per block-row and batch item, its rows in
+//                            slabs of R.  A slab's piece of every listed block
+//                            (R * block contiguous elements per operand) is
+//                            gathered into shared memory with 16-byte
 //                            asynchronous copies, each row's sum(y * dy) is
 //                            reduced there, and dx is written from the staged
-//                            copy: HBM sees 2 reads and 1 write per element.
+//                            copy (HBM sees 2 reads and 1 write per element);
+//                            two stages overlap the next slab's copies with
+//                            the current slab's work.
 //   bsr_bwd_unstaged_kernel  rows too long to stage: one CTA per row, the sum
 //                            in a first pass over global memory and dx in a
 //                            second (the re-read mostly served by L2).
@@ -40,9 +42,11 @@ struct BsrArgs {
     int64_t nbr;      // block-rows (table headers)
     int64_t nblocks;  // blocks per batch item
     int log2_block;
-    int log2_R;       // staged: rows per CTA = 2^log2_R (divides block, <= 64)
+    int log2_R;       // staged: a stage holds sizemax blocks of 2^log2_R rows per operand
+    int max_log2_R;   // staged: largest rows per slab, log2 (<= log2_block, <= log2(NT / 4))
     int sizemax;      // largest valid size of a block-row
     int ids_bytes;    // staged: shared bytes reserved for the block ids (multiple of 16)
+    int stage_bytes;  // staged: bytes of one stage (y slab, dy slab; multiple of 16)
     float scale;
 };
 
@@ -51,9 +55,20 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait for every committed group but the most recent one.
+__device__ __forceinline__ void cp_async_wait_prior()
+{
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all()
 {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 template <int N>
@@ -95,6 +110,10 @@ __device__ __forceinline__ int bsr_header(const BsrArgs &a, int64_t rbm, int32_t
     return bad ? -1 : size;
 }
 
+// One CTA per task t = z * nbr + rbm (one block-row of one batch item).  The
+// table entry is read once; the block-row's rows then stream, a slab of
+// several rows at a time, through two shared-memory stages: slab s + 1 is in
+// flight while slab s is reduced and written.
 // VEC: elements per access, 16 / sizeof(T) (16-byte vectors) or 1.
 template <typename T, int VEC, int NT>
 __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
@@ -109,17 +128,10 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
     __shared__ float s_row[NT / 4];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int log2_slabs = a.log2_block - a.log2_R;
-    const int64_t u = blockIdx.x;
-    const int64_t slab = u & ((int64_t{1} << log2_slabs) - 1);
-    const int64_t t = u >> log2_slabs;
-    const int64_t rbm = t % a.nbr;
-    const int64_t z = t / a.nbr;
-    const int log2_seg = a.log2_R + a.log2_block;  // elements of one block's slab
+    const int64_t task = blockIdx.x;
+    const int64_t rbm = task % a.nbr;
+    const int64_t z = task / a.nbr;
     int32_t *ids = reinterpret_cast<int32_t *>(smem);
-    T *ybuf = reinterpret_cast<T *>(smem + a.ids_bytes);
-    T *dybuf = ybuf + (static_cast<int64_t>(a.sizemax) << log2_seg);
-
     if (warp == 0) {
         int off;
         const int size = bsr_header(a, rbm, ids, lane, off);
@@ -134,97 +146,126 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
     if (size <= 0)
         return;
 
-    // gather: piece k of the slab = R rows of block ids[k], contiguous in global memory
+    // A stage holds sizemax blocks of 2^log2_R rows per operand; a block-row of
+    // `size` blocks takes slabs of 2^lr rows, the most that fit (at most
+    // 2^max_log2_R, the block's rows or NT / 4).
+    const int64_t seg_elems = static_cast<int64_t>(a.sizemax) << (a.log2_R + a.log2_block);
+    int lr = a.log2_R;
+    while (lr < a.max_log2_R && (int64_t{size} << (lr + 1)) <= (int64_t{a.sizemax} << a.log2_R))
+        ++lr;
+    const int log2_seg = lr + a.log2_block;  // elements of one block's slab
     const int64_t bb = int64_t{1} << (2 * a.log2_block);
-    const int64_t slab_off = slab << log2_seg;
-    const T *yb = static_cast<const T *>(a.y) + z * a.ys + slab_off;
-    const T *dyb = static_cast<const T *>(a.dy) + z * a.dys + slab_off;
-    const uint32_t ys_addr = smem_addr(ybuf), ds_addr = smem_addr(dybuf);
-    if constexpr (VEC > 1) {
-        const int log2_segv = log2_seg - LV;
-        const int nvec = size << log2_segv;
-        for (int q = tid; q < nvec; q += NT) {
-            const int k = q >> log2_segv;
-            const int w = q & ((1 << log2_segv) - 1);
-            const int64_t src = ids[k] * bb + (int64_t{w} << LV);
-            cp_async_16(ys_addr + 16u * q, yb + src);
-            cp_async_16(ds_addr + 16u * q, dyb + src);
-        }
-        cp_async_wait_all();
-    } else {
-        const int n = size << log2_seg;
-        for (int q = tid; q < n; q += NT) {
-            const int k = q >> log2_seg;
-            const int w = q & ((1 << log2_seg) - 1);
-            const int64_t src = ids[k] * bb + w;
-            ybuf[q] = yb[src];
-            dybuf[q] = dyb[src];
-        }
-    }
-    __syncthreads();
+    const int nslab = 1 << (a.log2_block - lr);
+    const T *ybase = static_cast<const T *>(a.y) + z * a.ys;
+    const T *dybase = static_cast<const T *>(a.dy) + z * a.dys;
+    T *xbase = static_cast<T *>(a.dx) + z * a.dxs;
+    auto ybuf = [&](int st) {
+        return reinterpret_cast<T *>(smem + a.ids_bytes + st * a.stage_bytes);
+    };
 
-    // row r of the slab is served by 2^log2_tpr consecutive threads
-    const int log2_tpr = LNT - a.log2_R;
+    // Gather slab sl into stage st: piece k = R rows of block ids[k],
+    // contiguous in global memory (16-byte asynchronous copies).
+    auto issue = [&](int sl, int st) {
+        const int64_t slab_off = int64_t{sl} << log2_seg;
+        T *yb = ybuf(st);
+        T *db = yb + seg_elems;
+        if constexpr (VEC > 1) {
+            const uint32_t ys_addr = smem_addr(yb), ds_addr = smem_addr(db);
+            const int log2_segv = log2_seg - LV;
+            const int nvec = size << log2_segv;
+            for (int q = tid; q < nvec; q += NT) {
+                const int64_t src = slab_off + ids[q >> log2_segv] * bb +
+                                    (int64_t{q & ((1 << log2_segv) - 1)} << LV);
+                cp_async_16(ys_addr + 16u * q, ybase + src);
+                cp_async_16(ds_addr + 16u * q, dybase + src);
+            }
+        } else {
+            const int n = size << log2_seg;
+            for (int q = tid; q < n; q += NT) {
+                const int64_t src = slab_off + ids[q >> log2_seg] * bb + (q & ((1 << log2_seg) - 1));
+                yb[q] = ybase[src];
+                db[q] = dybase[src];
+            }
+        }
+    };
+
+    // row r of a slab is served by 2^log2_tpr consecutive threads
+    const int log2_tpr = LNT - lr;
     const int tpr = 1 << log2_tpr;
     const int r = tid >> log2_tpr;
     const int part = tid & (tpr - 1);
     const int log2_bv = a.log2_block - LV;  // accesses per row of one block
     const int rv = size << log2_bv;         // accesses per matrix row
-    float acc = 0.f;
-    for (int j = part; j < rv; j += tpr) {
-        const int k = j >> log2_bv;
-        const int c = j & ((1 << log2_bv) - 1);
-        const int e = (((k << a.log2_R) + r) << a.log2_block) + (c << LV);
-        if constexpr (VEC > 1) {
-            float fy[VEC], fd[VEC];
-            E::unpack(ld_shared_v4(ys_addr + e * static_cast<uint32_t>(sizeof(T))), fy);
-            E::unpack(ld_shared_v4(ds_addr + e * static_cast<uint32_t>(sizeof(T))), fd);
-#pragma unroll
-            for (int i = 0; i < VEC; ++i)
-                acc = fmaf(fy[i], fd[i], acc);
-        } else {
-            acc = fmaf(E::load(ybuf + e), E::load(dybuf + e), acc);
-        }
-    }
-    if (tpr <= 32) {
-        for (int o = tpr >> 1; o > 0; o >>= 1)
-            acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (part == 0)
-            s_row[r] = acc;
-    } else {
-        acc = warp_sum(acc);
-        if (lane == 0)
-            s_warp[warp] = acc;
-        __syncthreads();
-        if (part == 0) {
-            float s = 0.f;
-            for (int i = 0; i < (tpr >> 5); ++i)
-                s += s_warp[warp + i];
-            s_row[r] = s;
-        }
-    }
-    __syncthreads();
-    const float sr = s_row[r];
     const float scale = a.scale;
 
-    T *xb = static_cast<T *>(a.dx) + z * a.dxs + slab_off + (int64_t{r} << a.log2_block);
-    for (int j = part; j < rv; j += tpr) {
-        const int k = j >> log2_bv;
-        const int c = j & ((1 << log2_bv) - 1);
-        const int e = (((k << a.log2_R) + r) << a.log2_block) + (c << LV);
-        T *dst = xb + ids[k] * bb + (c << LV);
-        if constexpr (VEC > 1) {
-            float fy[VEC], fd[VEC];
-            E::unpack(ld_shared_v4(ys_addr + e * static_cast<uint32_t>(sizeof(T))), fy);
-            E::unpack(ld_shared_v4(ds_addr + e * static_cast<uint32_t>(sizeof(T))), fd);
+    issue(0, 0);
+    cp_async_commit();
+    for (int sl = 0; sl < nslab; ++sl) {
+        const int st = sl & 1;
+        if (sl + 1 < nslab)
+            issue(sl + 1, st ^ 1);
+        cp_async_commit();
+        cp_async_wait_prior();  // all but the group just committed: slab sl has landed
+        __syncthreads();
+
+        const T *yb = ybuf(st);
+        const T *db = yb + seg_elems;
+        const uint32_t ys_addr = smem_addr(yb), ds_addr = smem_addr(db);
+        float acc = 0.f;
+        for (int j = part; j < rv; j += tpr) {
+            const int e = ((((j >> log2_bv) << lr) + r) << a.log2_block) +
+                          ((j & ((1 << log2_bv) - 1)) << LV);
+            if constexpr (VEC > 1) {
+                float fy[VEC], fd[VEC];
+                E::unpack(ld_shared_v4(ys_addr + e * static_cast<uint32_t>(sizeof(T))), fy);
+                E::unpack(ld_shared_v4(ds_addr + e * static_cast<uint32_t>(sizeof(T))), fd);
 #pragma unroll
-            for (int i = 0; i < VEC; ++i)
-                fy[i] = fy[i] * (fd[i] - sr) * scale;
-            __stcs(reinterpret_cast<uint4 *>(dst), E::pack(fy));
-        } else {
-            E::store(dst, E::load(ybuf + e) * (E::load(dybuf + e) - sr) * scale);
+                for (int i = 0; i < VEC; ++i)
+                    acc = fmaf(fy[i], fd[i], acc);
+            } else {
+                acc = fmaf(E::load(yb + e), E::load(db + e), acc);
+            }
         }
+        if (tpr <= 32) {
+            for (int o = tpr >> 1; o > 0; o >>= 1)
+                acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (part == 0)
+                s_row[r] = acc;
+        } else {
+            acc = warp_sum(acc);
+            if (lane == 0)
+                s_warp[warp] = acc;
+            __syncthreads();
+            if (part == 0) {
+                float sum = 0.f;
+                for (int i = 0; i < (tpr >> 5); ++i)
+                    sum += s_warp[warp + i];
+                s_row[r] = sum;
+            }
+        }
+        __syncthreads();
+        const float sr = s_row[r];
+        T *xb = xbase + (int64_t{sl} << log2_seg) + (int64_t{r} << a.log2_block);
+        for (int j = part; j < rv; j += tpr) {
+            const int k = j >> log2_bv;
+            const int c = j & ((1 << log2_bv) - 1);
+            const int e = (((k << lr) + r) << a.log2_block) + (c << LV);
+            T *dst = xb + ids[k] * bb + (c << LV);
+            if constexpr (VEC > 1) {
+                float fy[VEC], fd[VEC];
+                E::unpack(ld_shared_v4(ys_addr + e * static_cast<uint32_t>(sizeof(T))), fy);
+                E::unpack(ld_shared_v4(ds_addr + e * static_cast<uint32_t>(sizeof(T))), fd);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i)
+                    fy[i] = fy[i] * (fd[i] - sr) * scale;
+                __stcs(reinterpret_cast<uint4 *>(dst), E::pack(fy));
+            } else {
+                E::store(dst, E::load(yb + e) * (E::load(db + e) - sr) * scale);
+            }
+        }
+        __syncthreads();  // stage st and s_row are free for slab sl + 2
     }
+    cp_async_wait_all();
 }
 
 // One CTA per matrix row: u = (z * nbr + rbm) * block + rxm.

@@ -27,9 +27,9 @@ constexpr int kRingWarps = 16;                // consumer warps of the ring kern
 constexpr int kRingVpt1 = 4;                  // vectors per consumer thread and slot, one operand
 constexpr int kRingVpt2 = 2;                  // the same, two operands (softmax backward)
 constexpr int64_t kL2Budget = 56ll << 20;     // bytes of rows between their two reads, all SMs
-constexpr int64_t kBsrTarget = 48 * 1024;     // block-sparse: staged bytes per CTA aimed at
+constexpr int64_t kBsrTarget = 32 * 1024;     // block-sparse: bytes per slab stage aimed at
 constexpr int kBsrThreads = 256;              // block-sparse kernels' CTA size
-constexpr int kBsrMaxRows = 64;               // rows per staged CTA (<= kBsrThreads / 4)
+constexpr int kBsrMaxRows = 64;               // rows per slab (<= kBsrThreads / 4)
 
 size_t elem_size(int dtype) { return dtype == GBCE_F32 ? 4 : 2; }
 
@@ -515,8 +515,9 @@ int ce_call(void *logits, int64_t stride, const int64_t *targets, float *loss, f
 struct BsrPlan {
     bool staged;     // bsr_bwd_staged_kernel, else bsr_bwd_unstaged_kernel
     bool vec;        // 16-byte accesses, else one element at a time
-    int log2_R;      // staged: rows per CTA = 2^log2_R
+    int log2_R;      // staged: rows per slab = 2^log2_R
     int ids_bytes;   // staged: shared bytes for the block ids
+    int stage_bytes; // staged: one of the two slab stages
     int64_t smem;    // staged: dynamic shared memory per CTA
 };
 
@@ -528,10 +529,10 @@ int log2_exact(int64_t v)
     return l;
 }
 
-// Rows of sizemax * block elements: stage R rows per CTA (both operands and
-// the block ids in shared memory), R the largest power of two <= min(block,
-// kBsrMaxRows) within kBsrTarget bytes (one row at least, up to kSliceMax);
-// rows beyond kSliceMax go to the unstaged kernel.  `aligned`: the operands'
+// Rows of sizemax * block elements.  Staged when the block ids and two stages
+// of one row each (both operands) fit kSliceMax; R = the largest power of two
+// <= min(block, kBsrMaxRows) whose stage stays within kBsrTarget (one row at
+// least).  Longer rows go to the unstaged kernel.  `aligned`: the operands'
 // bases and batch strides allow 16-byte accesses.
 BsrPlan make_bsr_plan(int64_t block, int64_t sizemax, size_t es, bool aligned)
 {
@@ -540,17 +541,20 @@ BsrPlan make_bsr_plan(int64_t block, int64_t sizemax, size_t es, bool aligned)
     p.vec = aligned && block * static_cast<int64_t>(es) >= 16;
     p.ids_bytes = static_cast<int>((sizemax * 4 + 15) / 16 * 16);
     const int64_t row2 = sizemax * block * static_cast<int64_t>(es) * 2;
-    if (p.ids_bytes + row2 > kSliceMax) {
+    auto stage = [&](int l) { return ((row2 << l) + 15) / 16 * 16; };
+    if (p.ids_bytes + 2 * stage(0) > kSliceMax) {
         p.staged = false;
         return p;
     }
     p.staged = true;
-    const int64_t budget = kBsrTarget > p.ids_bytes + row2 ? kBsrTarget : p.ids_bytes + row2;
+    const int64_t budget = kBsrTarget > stage(0) ? kBsrTarget : stage(0);
     int l = 0;
-    while (l < log2_block && (1 << (l + 1)) <= kBsrMaxRows && p.ids_bytes + (row2 << (l + 1)) <= budget)
+    while (l < log2_block && (1 << (l + 1)) <= kBsrMaxRows && stage(l + 1) <= budget &&
+           p.ids_bytes + 2 * stage(l + 1) <= kSliceMax)
         ++l;
     p.log2_R = l;
-    p.smem = p.ids_bytes + (row2 << l);
+    p.stage_bytes = static_cast<int>(stage(l));
+    p.smem = p.ids_bytes + 2 * int64_t{p.stage_bytes};
     return p;
 }
 
@@ -928,8 +932,9 @@ extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
                     (dx_zstride * static_cast<int64_t>(es)) % 16 == 0));
     const BsrPlan p = make_bsr_plan(block, sizemax, es, aligned);
     const int log2_block = log2_exact(block);
-    const int per_row_block = p.staged ? log2_block - p.log2_R : log2_block;
-    // units = Z * n_block_rows * 2^per_row_block must fit a 1-D grid
+    const int per_row_block = p.staged ? 0 : log2_block;
+    // CTAs = Z * n_block_rows * 2^per_row_block must fit a 1-D grid (staged:
+    // one per block-row and batch item; unstaged: one per row)
     const int64_t kGridMax = INT32_MAX;
     if (n_block_rows > (kGridMax >> per_row_block) ||
         Z > (kGridMax >> per_row_block) / n_block_rows)
@@ -952,6 +957,9 @@ extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
     a.sizemax = static_cast<int>(sizemax);
     a.ids_bytes = p.ids_bytes;
     a.scale = scale;
+
+    a.stage_bytes = p.stage_bytes;
+    a.max_log2_R = log2_block < log2_exact(kBsrMaxRows) ? log2_block : log2_exact(kBsrMaxRows);
 
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);

@@ -218,6 +218,8 @@ def test_bsr_rejects_bad_arguments(lib, kw, code):
     (16, 2, 0, 1, "bsr_bwd_staged_kernel", 16),        # tiny rows: as many as the block has
     (128, 1, 2, 1, "bsr_bwd_staged_kernel", 64),       # capped at 64 rows per CTA
     (32, 1000, 0, 1, "bsr_bwd_unstaged_kernel", 1),    # 256 KB per row: not staged
+    (32, 390, 0, 1, "bsr_bwd_staged_kernel", 1),       # two stages of 101 KB fit 200 KB
+    (32, 400, 0, 1, "bsr_bwd_unstaged_kernel", 1),     # two stages of 104 KB do not
     (2, 3, 0, 1, "bsr_bwd_staged_kernel (element accesses)", 2),   # 8-byte block rows
     (32, 8, 1, 0, "bsr_bwd_staged_kernel (element accesses)", 32),
 ])

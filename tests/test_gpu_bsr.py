@@ -228,6 +228,8 @@ def test_bsr_bad_table(how, long_rows):
     lay[0, 2, :nb // 2] = True
     y, dy, lut, meta, _ = _layout_inputs(lay, block, dtype, 2, 9)
     nbr, nblocks, sizemax = meta["n_block_rows"], meta["nblocks"], meta["sizemax"]
+    kernel = gbce.bsr_plan(block, sizemax, dtype)[0]
+    assert kernel == ("bsr_bwd_unstaged_kernel" if long_rows else "bsr_bwd_staged_kernel")
     lut_h = lut.numpy()
     bad_lut = lut_h.copy()
     r = 2
