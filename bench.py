@@ -41,6 +41,8 @@ L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "cross_entropy_loss_ce_gb300", "csrc", f)
                   for f in ("row_kernels.cuh", "device.cuh")]
+BSR_KERNEL_SOURCES = [os.path.join(ROOT, "cross_entropy_loss_ce_gb300", "csrc", f)
+                      for f in ("bsr_kernels.cuh", "device.cuh")]
 
 
 # ---------------------------------------------------------------------------
@@ -77,25 +79,26 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(paths=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in paths:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the row kernel from the committed ncu summary,
-    or None when there is none or the kernel source changed since."""
-    path = os.path.join(PROFILE_DIR, f"ce_rows_{workload}.txt")
+def profiled_traffic(workload: str, prefix: str = "ce_rows", paths=KERNEL_SOURCES):
+    """DRAM bytes per launch of a kernel from the committed ncu summary
+    profiles/<prefix>_<workload>.txt, or None when there is none or the kernel
+    source changed since."""
+    path = os.path.join(PROFILE_DIR, f"{prefix}_{workload}.txt")
     try:
         text = open(path).read()
     except OSError:
         return None
     src = re.search(r"kernel_source_sha256_16:\s*(\w+)", text)
     val = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
-    if not src or not val or src.group(1) != kernel_source_hash():
+    if not src or not val or src.group(1) != kernel_source_hash(paths):
         return None
     return float(val.group(1))
 
@@ -355,13 +358,16 @@ def bsr_algorithmic_bytes(meta, Z, es, lut_len) -> int:
     return 3 * Z * meta["nblocks"] * meta["block"] ** 2 * es + 4 * lut_len
 
 
-def time_bsr(steps, warmup, ws, flush, peak):
+def time_bsr(steps, warmup, ws, flush, peak, heads=0):
     """Block-sparse softmax backward on each block-sparse workload (dx out of
     place, so every step sees the same inputs): kernel time from the library's
-    events, L2 flushed before each call."""
+    events, L2 flushed before each call.  ``heads`` > 0 keeps that many heads
+    of each workload (a smaller case for profiling)."""
     import cross_entropy_loss_ce_gb300 as gbce
     out = []
     for w in workloads.BSR_WORKLOADS.values():
+        if heads:
+            w = w.with_sizes(H=heads)
         y, dy, lut, meta = workloads.make_bsr_inputs(w, device="cuda")
         dx = torch.empty_like(dy)
         call = lambda: gbce.softmax_bwd_bsr(y, dy, lut, meta["n_block_rows"], meta["nblocks"],
@@ -384,10 +390,13 @@ def time_bsr(steps, warmup, ws, flush, peak):
         b = bsr_algorithmic_bytes(meta, w.Z, esize(w.dtype), lut.numel())
         rows = w.Z * meta["n_block_rows"] * meta["block"]
         kernel, R = gbce.bsr_plan(meta["block"], meta["sizemax"], w.dtype)
-        out.append({"workload": w.name, "kernel": kernel, "rows_per_cta": R,
+        out.append({"workload": w.name + (f" ({heads} heads)" if heads else ""),
+                    "kernel": kernel, "rows_per_cta": R,
                     "timing": "kernel, CUDA events", "kernel_ms": ms,
                     "rows_per_s": rows / (ms / 1e3), "algorithmic_bytes": b,
-                    "gbs": b / (ms / 1e3) / 1e9, "frac": b / (ms / 1e3) / 1e9 / peak})
+                    "gbs": b / (ms / 1e3) / 1e9, "frac": b / (ms / 1e3) / 1e9 / peak,
+                    "traffic": None if heads else profiled_traffic(
+                        w.name, "softmax_bwd_bsr", BSR_KERNEL_SOURCES)})
         del y, dy, dx
         torch.cuda.empty_cache()
     return out
@@ -531,6 +540,18 @@ def run_table(args, local):
                           "rows_per_cta": r["rows_per_cta"]}), flush=True)
 
 
+def run_bsr(args, local):
+    """--bsr: kernel-only time of the block-sparse softmax backward workloads
+    (one JSON line per workload)."""
+    import cross_entropy_loss_ce_gb300 as gbce
+    gbce.load_library()
+    torch.cuda.set_device(local)
+    peak, _ = measured_peaks()
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for r in time_bsr(args.steps, args.warmup, 1, flush, peak, args.bsr_heads):
+        print(json.dumps(r), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -546,6 +567,10 @@ def main():
     ap.add_argument("--no-softmax", action="store_true",
                     help="skip the row softmax and block-sparse softmax backward timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bsr", action="store_true",
+                    help="time only the block-sparse softmax backward workloads")
+    ap.add_argument("--bsr-heads", type=int, default=0,
+                    help="with --bsr: keep this many heads of each workload (profiling)")
     ap.add_argument("--table", action="store_true",
                     help="print the kernel time of every workload instead of the benchmark line")
     args = ap.parse_args()
@@ -562,6 +587,8 @@ def main():
             run_reference(args, ws, rank)
         elif args.table:
             run_table(args, local)
+        elif args.bsr:
+            run_bsr(args, local)
         else:
             run_gbce(args, ws, rank, local)
     finally:

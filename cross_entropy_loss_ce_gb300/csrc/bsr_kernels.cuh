@@ -16,8 +16,8 @@
 //                            asynchronous copies, each row's sum(y * dy) is
 //                            reduced there, and dx is written from the staged
 //                            copy (HBM sees 2 reads and 1 write per element);
-//                            two stages overlap the next slab's copies with
-//                            the current slab's work.
+//                            stages overlap the next slabs' copies with the
+//                            current slab's work.
 //   bsr_bwd_unstaged_kernel  rows too long to stage: one CTA per row, the sum
 //                            in a first pass over global memory and dx in a
 //                            second (the re-read mostly served by L2).
@@ -60,10 +60,11 @@ __device__ __forceinline__ void cp_async_commit()
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Wait for every committed group but the most recent one.
-__device__ __forceinline__ void cp_async_wait_prior()
+// Wait until at most N committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pending()
 {
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_wait_all()
@@ -112,10 +113,11 @@ __device__ __forceinline__ int bsr_header(const BsrArgs &a, int64_t rbm, int32_t
 
 // One CTA per task t = z * nbr + rbm (one block-row of one batch item).  The
 // table entry is read once; the block-row's rows then stream, a slab of
-// several rows at a time, through two shared-memory stages: slab s + 1 is in
-// flight while slab s is reduced and written.
-// VEC: elements per access, 16 / sizeof(T) (16-byte vectors) or 1.
-template <typename T, int VEC, int NT>
+// several rows at a time, through STAGES shared-memory stages: slabs s + 1 ..
+// s + STAGES - 1 are in flight while slab s is reduced and written.
+// VEC: elements per access, 16 / sizeof(T) (16-byte vectors) or 1.  STAGES:
+// slab stages in shared memory (STAGES - 1 slabs in flight during the work).
+template <typename T, int VEC, int NT, int STAGES>
 __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
 {
     using E = Elem<T>;
@@ -198,14 +200,17 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
     const int rv = size << log2_bv;         // accesses per matrix row
     const float scale = a.scale;
 
-    issue(0, 0);
-    cp_async_commit();
-    for (int sl = 0; sl < nslab; ++sl) {
-        const int st = sl & 1;
-        if (sl + 1 < nslab)
-            issue(sl + 1, st ^ 1);
+    for (int sl = 0; sl < STAGES - 1; ++sl) {
+        if (sl < nslab)
+            issue(sl, sl);
         cp_async_commit();
-        cp_async_wait_prior();  // all but the group just committed: slab sl has landed
+    }
+    for (int sl = 0; sl < nslab; ++sl) {
+        const int st = sl % STAGES;
+        if (sl + STAGES - 1 < nslab)
+            issue(sl + STAGES - 1, (sl + STAGES - 1) % STAGES);
+        cp_async_commit();
+        cp_async_wait_pending<STAGES - 1>();  // slab sl has landed
         __syncthreads();
 
         const T *yb = ybuf(st);
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
                 E::store(dst, E::load(yb + e) * (E::load(db + e) - sr) * scale);
             }
         }
-        __syncthreads();  // stage st and s_row are free for slab sl + 2
+        __syncthreads();  // stage st and s_row are free for slab sl + STAGES
     }
     cp_async_wait_all();
 }

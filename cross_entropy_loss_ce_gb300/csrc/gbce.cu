@@ -30,6 +30,7 @@ constexpr int64_t kL2Budget = 56ll << 20;     // bytes of rows between their two
 constexpr int64_t kBsrTarget = 32 * 1024;     // block-sparse: bytes per slab stage aimed at
 constexpr int kBsrThreads = 256;              // block-sparse kernels' CTA size
 constexpr int kBsrMaxRows = 64;               // rows per slab (<= kBsrThreads / 4)
+constexpr int kBsrStages = 2;                 // slab stages in shared memory
 
 size_t elem_size(int dtype) { return dtype == GBCE_F32 ? 4 : 2; }
 
@@ -517,7 +518,7 @@ struct BsrPlan {
     bool vec;        // 16-byte accesses, else one element at a time
     int log2_R;      // staged: rows per slab = 2^log2_R
     int ids_bytes;   // staged: shared bytes for the block ids
-    int stage_bytes; // staged: one of the two slab stages
+    int stage_bytes; // staged: one of the kBsrStages slab stages
     int64_t smem;    // staged: dynamic shared memory per CTA
 };
 
@@ -529,8 +530,8 @@ int log2_exact(int64_t v)
     return l;
 }
 
-// Rows of sizemax * block elements.  Staged when the block ids and two stages
-// of one row each (both operands) fit kSliceMax; R = the largest power of two
+// Rows of sizemax * block elements.  Staged when the block ids and kBsrStages
+// stages of one row each (both operands) fit kSliceMax; R = the largest power of two
 // <= min(block, kBsrMaxRows) whose stage stays within kBsrTarget (one row at
 // least).  Longer rows go to the unstaged kernel.  `aligned`: the operands'
 // bases and batch strides allow 16-byte accesses.
@@ -542,7 +543,7 @@ BsrPlan make_bsr_plan(int64_t block, int64_t sizemax, size_t es, bool aligned)
     p.ids_bytes = static_cast<int>((sizemax * 4 + 15) / 16 * 16);
     const int64_t row2 = sizemax * block * static_cast<int64_t>(es) * 2;
     auto stage = [&](int l) { return ((row2 << l) + 15) / 16 * 16; };
-    if (p.ids_bytes + 2 * stage(0) > kSliceMax) {
+    if (p.ids_bytes + kBsrStages * stage(0) > kSliceMax) {
         p.staged = false;
         return p;
     }
@@ -550,11 +551,11 @@ BsrPlan make_bsr_plan(int64_t block, int64_t sizemax, size_t es, bool aligned)
     const int64_t budget = kBsrTarget > stage(0) ? kBsrTarget : stage(0);
     int l = 0;
     while (l < log2_block && (1 << (l + 1)) <= kBsrMaxRows && stage(l + 1) <= budget &&
-           p.ids_bytes + 2 * stage(l + 1) <= kSliceMax)
+           p.ids_bytes + kBsrStages * stage(l + 1) <= kSliceMax)
         ++l;
     p.log2_R = l;
     p.stage_bytes = static_cast<int>(stage(l));
-    p.smem = p.ids_bytes + 2 * int64_t{p.stage_bytes};
+    p.smem = p.ids_bytes + kBsrStages * int64_t{p.stage_bytes};
     return p;
 }
 
@@ -565,8 +566,8 @@ BsrFn pick_bsr_t(const BsrPlan &p)
 {
     constexpr int V = 16 / sizeof(T);
     if (p.staged)
-        return p.vec ? bsr_bwd_staged_kernel<T, V, kBsrThreads>
-                     : bsr_bwd_staged_kernel<T, 1, kBsrThreads>;
+        return p.vec ? bsr_bwd_staged_kernel<T, V, kBsrThreads, kBsrStages>
+                     : bsr_bwd_staged_kernel<T, 1, kBsrThreads, kBsrStages>;
     return p.vec ? bsr_bwd_unstaged_kernel<T, V, kBsrThreads>
                  : bsr_bwd_unstaged_kernel<T, 1, kBsrThreads>;
 }
