@@ -276,8 +276,8 @@ def softmax_bwd_bsr(y: torch.Tensor, dy: torch.Tensor, lut: torch.Tensor, n_bloc
 
 
 def bsr_plan(block: int, sizemax: int, dtype: torch.dtype, aligned: bool = True):
-    """(kernel name, rows per CTA) softmax_bwd_bsr uses for this block size,
-    longest block-row and dtype."""
+    """(kernel name, rows per slab of a block-row of sizemax blocks) that
+    softmax_bwd_bsr uses for this block size, longest block-row and dtype."""
     r = ctypes.c_int(0)
     name = load_library().gbce_bsr_plan(block, sizemax, DTYPES[dtype], 1 if aligned else 0,
                                         ctypes.byref(r))

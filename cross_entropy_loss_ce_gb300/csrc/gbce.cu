@@ -976,13 +976,13 @@ extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
 }
 
 extern "C" const char *gbce_bsr_plan(int64_t block, int64_t sizemax, int dtype, int aligned,
-                                     int *rows_per_cta)
+                                     int *rows_per_slab)
 {
     if (check_bsr_shape(0, 0, 0, 0, 0, 0, block, sizemax, 0, dtype) != GBCE_OK || sizemax < 1)
         return nullptr;
     const BsrPlan p = make_bsr_plan(block, sizemax, elem_size(dtype), aligned != 0);
-    if (rows_per_cta)
-        *rows_per_cta = p.staged ? 1 << p.log2_R : 1;
+    if (rows_per_slab)
+        *rows_per_slab = p.staged ? 1 << p.log2_R : 1;
     if (p.staged)
         return p.vec ? "bsr_bwd_staged_kernel" : "bsr_bwd_staged_kernel (element accesses)";
     return p.vec ? "bsr_bwd_unstaged_kernel" : "bsr_bwd_unstaged_kernel (element accesses)";

@@ -244,14 +244,16 @@ GBCE_API int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy, i
 
 /*
  * gbce_bsr_plan -- the kernel softmax_bwd_bsr uses for `block`, `sizemax` and
- * `dtype` ("bsr_bwd_staged_kernel": slabs of *rows_per_cta rows of a
- * block-row staged in shared memory; "bsr_bwd_unstaged_kernel": one row per
- * CTA, two passes over global memory; " (element accesses)" appended when
- * `aligned` is 0 or a block row is under 16 bytes).  NULL for invalid
- * arguments.  For tests and diagnostics; no kernel is launched.
+ * `dtype` ("bsr_bwd_staged_kernel": one CTA per block-row and batch item, its
+ * rows staged in shared memory a slab at a time, *rows_per_slab rows per slab
+ * for a block-row of sizemax blocks (shorter block-rows take more);
+ * "bsr_bwd_unstaged_kernel": one row per CTA, two passes over global memory,
+ * *rows_per_slab = 1; " (element accesses)" appended when `aligned` is 0 or a
+ * block row is under 16 bytes).  NULL for invalid arguments.  For tests and
+ * diagnostics; no kernel is launched.
  */
 GBCE_API const char *gbce_bsr_plan(int64_t block, int64_t sizemax, int dtype, int aligned,
-                                   int *rows_per_cta);
+                                   int *rows_per_slab);
 
 /*
  * gbce_plan -- the row-kernel family a call uses for rows of `cols` elements
