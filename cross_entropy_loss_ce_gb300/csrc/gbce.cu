@@ -19,6 +19,9 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kWarpMaxVpl = 16;               // rows of <= 32 * 16 16-byte vectors: warp kernel
 constexpr int64_t kResidentMax = 64 * 1024;   // rows up to this many staged bytes: resident kernel
+constexpr int64_t kResidentMaxFwd = 32 * 1024;  // the same for the softmax forward (measured: the
+                                               // ring streams 64 KB fp32 rows 3% faster there,
+                                               // while CE rows of 64 KB lose 17% on it)
 constexpr int64_t kSliceMax = 200 * 1024;     // dynamic shared memory limit set on every kernel
 constexpr int kMaxCluster = 16;
 constexpr int64_t kStreamSlice = 64 * 1024;   // bytes of a row per CTA in the streaming fallback
@@ -72,7 +75,8 @@ struct Plan {
 
 // cols elements of esize bytes per operand, nbuf operands per row; `aligned`:
 // all operands of every row share their address modulo 16 bytes.
-Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned)
+Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned,
+               int64_t resident_max = kResidentMax)
 {
     Plan p{};
     const int64_t row_bytes = cols * static_cast<int64_t>(esize);
@@ -96,7 +100,7 @@ Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned)
             p.vpl *= 2;
         return p;
     }
-    if (nvec * 16 * nbuf <= kResidentMax) {
+    if (nvec * 16 * nbuf <= resident_max) {
         // short rows: one CTA per row holds the row, three CTAs per SM
         p.kind = Kind::Resident;
         p.C = 1;
@@ -693,7 +697,8 @@ extern "C" int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_s
     if (M == 0)
         return GBCE_OK;
     const size_t es = elem_size(dtype);
-    const Plan p = make_plan(N, es, 1, same_phase(x, x_stride, y, y_stride, es, M));
+    const Plan p = make_plan(N, es, 1, same_phase(x, x_stride, y, y_stride, es, M),
+                             kResidentMaxFwd);
     RowArgs a{};
     a.in0 = x;
     a.s0 = x_stride;
@@ -749,7 +754,8 @@ extern "C" const char *gbce_plan(int op, int64_t cols, int dtype, int same_phase
     if (op < 0 || op > 2 || cols < 1 ||
         (dtype != GBCE_F32 && dtype != GBCE_BF16 && dtype != GBCE_F16))
         return nullptr;
-    const Plan p = make_plan(cols, elem_size(dtype), op == 2 ? 2 : 1, same_phase != 0);
+    const Plan p = make_plan(cols, elem_size(dtype), op == 2 ? 2 : 1, same_phase != 0,
+                             op == 1 ? kResidentMaxFwd : kResidentMax);
     if (ctas_per_row)
         *ctas_per_row = p.C;
     switch (p.kind) {

@@ -149,8 +149,9 @@ def test_empty_calls_are_noops(lib):
 
 def test_plan_picks_the_regime_by_row_length(lib):
     """Host-side plan (no device here, so no cluster split): warp rows up to
-    8 KB per operand, resident up to 64 KB staged, ring beyond, streaming when
-    operands' rows sit at different 16-byte phases."""
+    8 KB per operand, resident up to 64 KB staged (32 KB for the softmax
+    forward), ring beyond, streaming when operands' rows sit at different
+    16-byte phases."""
     lib.gbce_plan.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                               ctypes.POINTER(ctypes.c_int)]
     lib.gbce_plan.restype = ctypes.c_char_p
@@ -167,7 +168,9 @@ def test_plan_picks_the_regime_by_row_length(lib):
     assert plan(0, 32776, 1) == "rows_ring_kernel"
     assert plan(2, 8192, 0) == "rows_resident_kernel"      # two 32 KB operands: 64 KB
     assert plan(2, 8196, 0) == "rows_ring_kernel"
-    assert plan(1, 8192, 0) == "rows_resident_kernel"
+    assert plan(1, 8192, 0) == "rows_resident_kernel"      # softmax forward: 32 KB
+    assert plan(1, 8196, 0) == "rows_ring_kernel"
+    assert plan(1, 16384, 0) == "rows_ring_kernel"         # 64 KB fp32 forward rows
     assert plan(1, 8192, 0, same=0) == "rows_streaming_kernel"
     assert plan(0, 128256, 2) == "rows_ring_kernel"        # fp16
     assert lib.gbce_plan(3, 10, 0, 1, None) is None
