@@ -325,22 +325,19 @@ def time_ce(w, xd0, td, steps, warmup, ws, flush):
 
 
 def time_ce_e2e(w, x_pinned, t_pinned, steps, ws):
-    """End to end through the public call: pinned host -> device copy of the
-    step's logits and targets, the call, device -> host read of the loss."""
+    """End to end through the public host-buffer call ce_fwd_bwd_host: pinned
+    host -> device copies of the step's targets and logits (the logits in row
+    chunks that overlap the row kernels), the call, the loss read back into
+    pinned host memory."""
     import cross_entropy_loss_ce_gb300 as gbce
-    xd = torch.empty(x_pinned.shape, dtype=x_pinned.dtype, device="cuda")
-    td = torch.empty(t_pinned.shape, dtype=t_pinned.dtype, device="cuda")
-    loss = torch.empty((), dtype=torch.float32, device="cuda")
+    grad = torch.empty(x_pinned.shape, dtype=x_pinned.dtype, device="cuda")
     loss_host = torch.empty((), dtype=torch.float32).pin_memory()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     total = 0.0
     for i in range(steps + 1):
         barrier_sync(ws)
         start.record()
-        xd.copy_(x_pinned, non_blocking=True)
-        td.copy_(t_pinned, non_blocking=True)
-        gbce.ce_fwd_bwd(xd, td, workloads.IGNORE_INDEX, loss)
-        loss_host.copy_(loss, non_blocking=True)
+        gbce.ce_fwd_bwd_host(x_pinned, t_pinned, workloads.IGNORE_INDEX, grad, loss_host)
         stop.record()
         barrier_sync(ws)
         if i > 0:  # the first iteration is a warm-up

@@ -313,6 +313,51 @@ def timing_read():
     return ms.value, n.value
 
 
+def ce_fwd_bwd_host(logits_host: torch.Tensor, targets_host: torch.Tensor,
+                    ignore_index: int = -100, grad: torch.Tensor = None,
+                    loss_host: torch.Tensor = None, stream=None):
+    """ce_fwd_bwd from host memory: (grad, loss_host).
+
+    ``logits_host`` [M, V] and ``targets_host`` [M] (int64) are CPU tensors
+    (pinned memory makes the copies asynchronous).  ``grad`` is a CUDA tensor of
+    the logits' shape and dtype (allocated when not given) that receives the
+    logits and then, in place, the gradient; ``loss_host`` is a one-element
+    CPU float32 tensor (pinned when allocated here) that holds the mean loss
+    once the stream has reached the end of the call.
+    """
+    if logits_host.is_cuda or targets_host.is_cuda:
+        raise ValueError("logits_host and targets_host must be CPU tensors")
+    if logits_host.dim() != 2 or (logits_host.shape[1] > 1 and logits_host.stride(1) != 1):
+        raise ValueError("logits_host must be 2-D with unit column stride")
+    if logits_host.dtype not in DTYPES:
+        raise TypeError(f"logits_host must be float32, bfloat16 or float16, not {logits_host.dtype}")
+    M, V = logits_host.shape
+    if targets_host.dtype != torch.int64 or targets_host.shape != (M,) or \
+            not targets_host.is_contiguous():
+        raise ValueError("targets_host must be a contiguous int64 tensor of shape [M]")
+    hs = logits_host.stride(0) if M > 1 else V
+    if grad is None:
+        grad = torch.empty((M, V), dtype=logits_host.dtype, device="cuda")
+    gp, gs, Mg, Vg = _matrix(grad, "grad")
+    if (Mg, Vg) != (M, V) or grad.dtype != logits_host.dtype:
+        raise ValueError("grad must match the logits' shape and dtype")
+    if loss_host is None:
+        loss_host = torch.empty((), dtype=torch.float32).pin_memory()
+    elif loss_host.dtype != torch.float32 or loss_host.numel() != 1 or loss_host.is_cuda:
+        raise ValueError("loss_host must be a one-element float32 CPU tensor")
+    lib = load_library()
+    fn = lib.ce_fwd_bwd_host
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    rc = fn(logits_host.data_ptr(), max(hs, V), targets_host.data_ptr(), gp, gs,
+            loss_host.data_ptr(), M, V, int(ignore_index), DTYPES[logits_host.dtype],
+            _stream_handle(stream))
+    _check(rc, "ce_fwd_bwd_host")
+    return grad, loss_host
+
+
 def ce_fwd_bwd_noalloc(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = -100,
                        loss: torch.Tensor = None, stream=None) -> torch.Tensor:
     """ce_fwd_bwd for callers that cannot let the library allocate device memory.

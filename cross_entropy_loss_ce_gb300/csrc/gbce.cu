@@ -609,6 +609,117 @@ int check_bsr_shape(int64_t y_zstride, int64_t dy_zstride, int64_t dx_zstride, i
     return GBCE_OK;
 }
 
+// ---------------------------------------------------------------------------
+// the fused cross-entropy from host buffers: copies overlapped with the rows
+
+constexpr int kHostChunks = 8;  // row chunks whose copy overlaps the previous chunk's kernel
+
+std::mutex g_copy_mu;
+cudaStream_t g_copy_stream[kMaxDevices] = {};
+
+// The library's host-to-device copy stream of `device` (created once).
+cudaError_t copy_stream_for(int device, cudaStream_t *out)
+{
+    if (device < 0 || device >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_copy_mu);
+    if (!g_copy_stream[device]) {
+        cudaStream_t s;
+        cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+        if (e != cudaSuccess)
+            return e;
+        g_copy_stream[device] = s;
+    }
+    *out = g_copy_stream[device];
+    return cudaSuccess;
+}
+
+// Scratch of one host call: n and the device loss in the header, the row
+// losses at kCeScratchHeader, then the targets (8-byte aligned).
+cudaError_t launch_ce_host(const void *logits_host, int64_t host_stride,
+                           const int64_t *targets_host, void *grad, int64_t stride,
+                           float *loss_host, int64_t M, int64_t V, int64_t ignore_index,
+                           int dtype, void *scratch, cudaStream_t stream, cudaStream_t copy)
+{
+    const size_t es = elem_size(dtype);
+    int *n_ptr = static_cast<int *>(scratch);
+    float *loss_dev = reinterpret_cast<float *>(static_cast<char *>(scratch) + 16);
+    float *row_loss = reinterpret_cast<float *>(static_cast<char *>(scratch) + kCeScratchHeader);
+    int64_t *targets = reinterpret_cast<int64_t *>(
+        static_cast<char *>(scratch) + kCeScratchHeader + (static_cast<size_t>(M) * 4 + 7) / 8 * 8);
+    cudaError_t e = cudaSuccess;
+    if (M > 0)
+        e = cudaMemcpyAsync(targets, targets_host, static_cast<size_t>(M) * 8,
+                            cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess)
+        return e;
+    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr, loss_dev,
+                                                   GBCE_MEAN);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    if (M > 0) {
+        // the copies start once the stream's earlier work is done (grad may be in use)
+        cudaEvent_t ready = nullptr;
+        if ((e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming)) != cudaSuccess)
+            return e;
+        e = cudaEventRecord(ready, stream);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(copy, ready, 0);
+        cudaEventDestroy(ready);
+        if (e != cudaSuccess)
+            return e;
+        const Plan p = make_plan(V, es, 1, true);
+        const KernelFn fn = pick<Op::CE>(dtype, p);
+        const int64_t chunks = M < kHostChunks ? M : kHostChunks;
+        const int64_t per = (M + chunks - 1) / chunks;
+        for (int64_t r0 = 0; r0 < M; r0 += per) {
+            const int64_t rows = r0 + per < M ? per : M - r0;
+            char *dst = static_cast<char *>(grad) + r0 * stride * es;
+            const char *src = static_cast<const char *>(logits_host) + r0 * host_stride * es;
+            if (host_stride == V && stride == V)  // contiguous rows: one linear copy
+                e = cudaMemcpyAsync(dst, src, rows * V * es, cudaMemcpyHostToDevice, copy);
+            else
+                e = cudaMemcpy2DAsync(dst, stride * es, src, host_stride * es, V * es, rows,
+                                      cudaMemcpyHostToDevice, copy);
+            cudaEvent_t landed = nullptr;
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&landed, cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventRecord(landed, copy);
+            if (e == cudaSuccess)
+                e = cudaStreamWaitEvent(stream, landed, 0);
+            if (landed)
+                cudaEventDestroy(landed);
+            if (e != cudaSuccess)
+                return e;
+            RowArgs a{};
+            void *rows0 = static_cast<char *>(grad) + r0 * stride * es;
+            a.in0 = rows0;
+            a.s0 = stride;
+            a.out = rows0;
+            a.so = stride;
+            a.M = rows;
+            a.cols = V;
+            a.targets = targets + r0;
+            a.ignore_index = ignore_index;
+            a.n_ptr = n_ptr;
+            a.row_loss = row_loss + r0;
+            a.reduction = GBCE_MEAN;
+            a.grad_scale = nullptr;
+            a.C = p.C;
+            a.per_vec = p.per_vec;
+            a.chunk_vec = p.chunk_vec;
+            a.nslot = p.nslot;
+            if ((e = launch_rows(fn, p, a, stream)) != cudaSuccess)
+                return e;
+        }
+        ce_mean_kernel<1024><<<1, 1024, 0, stream>>>(row_loss, M, n_ptr, loss_dev, GBCE_MEAN);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+    }
+    return cudaMemcpyAsync(loss_host, loss_dev, sizeof(float), cudaMemcpyDeviceToHost, stream);
+}
+
 }  // namespace
 }  // namespace gbce
 
@@ -992,4 +1103,45 @@ extern "C" const char *gbce_bsr_plan(int64_t block, int64_t sizemax, int dtype, 
     if (p.staged)
         return p.vec ? "bsr_bwd_staged_kernel" : "bsr_bwd_staged_kernel (element accesses)";
     return p.vec ? "bsr_bwd_unstaged_kernel" : "bsr_bwd_unstaged_kernel (element accesses)";
+}
+
+extern "C" int ce_fwd_bwd_host(const void *logits_host, int64_t host_stride,
+                               const int64_t *targets_host, void *grad, int64_t stride,
+                               float *loss_host, int64_t M, int64_t V, int64_t ignore_index,
+                               int dtype, gbce_stream_t stream_)
+{
+    int st = check_common(M, V, dtype);
+    if (st)
+        return st;
+    if (!loss_host || (M > 0 && (!targets_host || !logits_host)))
+        return GBCE_ERR_NULL;
+    if (host_stride < V || host_stride > kMaxStride)
+        return GBCE_ERR_SIZE;
+    if ((st = check_matrix(grad, stride, M, V, dtype)))
+        return st;
+    const size_t es = elem_size(dtype);
+    if (!aligned_to(logits_host, es) || !aligned_to(targets_host, 8) || !aligned_to(loss_host, 4))
+        return GBCE_ERR_ALIGN;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess)
+        return map_error(e);
+    cudaStream_t copy;
+    if ((e = copy_stream_for(device, &copy)) != cudaSuccess)
+        return map_error(e);
+    cudaMemPool_t pool;
+    if ((e = pool_for(device, &pool)) != cudaSuccess)
+        return map_error(e);
+    void *scratch = nullptr;
+    const size_t bytes = kCeScratchHeader + (static_cast<size_t>(M) * 4 + 7) / 8 * 8 +
+                         static_cast<size_t>(M) * 8;
+    if ((e = cudaMallocFromPoolAsync(&scratch, bytes, pool, stream)) != cudaSuccess)
+        return map_error(e);
+    e = launch_ce_host(logits_host, host_stride, targets_host, grad, stride, loss_host, M, V,
+                       ignore_index, dtype, scratch, stream, copy);
+    cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e == cudaSuccess)
+        e = ef;
+    return map_error(e);
 }

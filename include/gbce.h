@@ -176,6 +176,31 @@ GBCE_API int ce_fwd_bwd_noalloc(void *logits, int64_t stride, const int64_t *tar
                                 gbce_stream_t stream);
 
 /*
+ * ce_fwd_bwd_host -- ce_fwd_bwd with the logits and targets in host memory
+ * and the loss returned to host memory: the end-to-end form of the call.
+ *
+ *   logits_host [M, host_stride] host memory, read (pinned memory makes the
+ *               copies asynchronous; pageable memory works, synchronously).
+ *   targets_host [M] int64, host memory, read.
+ *   grad        [M, stride] device memory, written: it receives the logits
+ *               and then, in place, d(loss)/d(logits) exactly as ce_fwd_bwd
+ *               writes them (columns 0..V-1 of each row).
+ *   loss_host   one float in host memory: the mean loss, written when the
+ *               stream reaches the end of the call (synchronise before reading).
+ * The logits are copied in up to 8 row chunks on a library-owned copy stream
+ * of the device; each chunk's row kernel waits only for its own chunk, so the
+ * copy of chunk k + 1 overlaps the kernel of chunk k.  The copies start after
+ * the work already enqueued on `stream`; the call's results are ordered before
+ * later work on `stream`.  Scratch (the targets, n, the row losses) comes from
+ * the same stream-ordered pool as ce_fwd_bwd.  Argument errors as ce_fwd_bwd,
+ * plus GBCE_ERR_SIZE for host_stride < V; device flags through gbce_last_error.
+ */
+GBCE_API int ce_fwd_bwd_host(const void *logits_host, int64_t host_stride,
+                             const int64_t *targets_host, void *grad, int64_t stride,
+                             float *loss_host, int64_t M, int64_t V, int64_t ignore_index,
+                             int dtype, gbce_stream_t stream);
+
+/*
  * softmax_fwd -- row-wise safe softmax, y = exp(x - max x) / sum exp(x - max x).
  *
  * Defined by: "python sum function examples (triton.language)", _softmax and

@@ -232,3 +232,24 @@ def test_bsr_plan(lib, block, sizemax, dtype, aligned, kernel, rows):
     assert name.decode() == kernel and r.value == rows
     assert lib.gbce_bsr_plan(3, 1, 0, 1, None) is None
     assert lib.gbce_bsr_plan(32, 0, 0, 1, None) is None
+
+
+# ce_fwd_bwd_host(logits_host, host_stride, targets_host, grad, stride, loss_host, M, V,
+#                 ignore_index, dtype)
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, 10, FAKE, FAKE, 10, None, 4, 10, -100, 0), 1),       # NULL loss_host
+    ((None, 10, FAKE, FAKE, 10, FAKE, 4, 10, -100, 0), 1),       # NULL logits_host
+    ((FAKE, 10, None, FAKE, 10, FAKE, 4, 10, -100, 0), 1),       # NULL targets_host
+    ((FAKE, 10, FAKE, None, 10, FAKE, 4, 10, -100, 0), 1),       # NULL grad
+    ((FAKE, 9, FAKE, FAKE, 10, FAKE, 4, 10, -100, 0), 2),        # host stride < V
+    ((FAKE, 10, FAKE, FAKE, 9, FAKE, 4, 10, -100, 0), 2),        # device stride < V
+    ((FAKE, 10, FAKE, FAKE, 10, FAKE, -1, 10, -100, 0), 2),      # M < 0
+    ((FAKE, 10, FAKE, FAKE, 10, FAKE, 4, 10, -100, 3), 3),       # unknown dtype
+    ((FAKE + 2, 10, FAKE, FAKE, 10, FAKE, 4, 10, -100, 0), 4),   # host logits misaligned
+    ((FAKE, 10, FAKE + 4, FAKE, 10, FAKE, 4, 10, -100, 0), 4),   # host targets misaligned
+    ((FAKE, 10, FAKE, FAKE, 10, FAKE + 2, 4, 10, -100, 0), 4),   # loss_host misaligned
+])
+def test_ce_host_rejects_bad_arguments(lib, args, code):
+    i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.ce_fwd_bwd_host.argtypes = [p, i64, p, p, i64, p, i64, i64, i64, ci, p]
+    assert lib.ce_fwd_bwd_host(*args, None) == code
