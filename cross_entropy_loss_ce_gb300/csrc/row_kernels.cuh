@@ -500,10 +500,6 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
     float pa, pb;  // (m, d) for CE / softmax fwd, (sum y*dy, unused) for softmax bwd
     if constexpr (OP == Op::SoftmaxBwd) {
         float sdot = 0.f;
-        if (head_here)
-            sdot = fmaf(h0, h1, sdot);
-        if (tail_here)
-            sdot = fmaf(t0, t1, sdot);
         for (int k = 0; k < nch && ok; ++k) {
             ok = mbar_wait_bounded(smem_addr(&bars[k]), 0);
             const int c1 = (k + 1) * a.chunk_vec < cnt ? (k + 1) * a.chunk_vec : cnt;
@@ -518,15 +514,17 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
                 }
             }
         }
+        // head and tail (loaded before the chunks landed) last: their load latency
+        // overlaps the chunk waits
+        if (head_here)
+            sdot = fmaf(h0, h1, sdot);
+        if (tail_here)
+            sdot = fmaf(t0, t1, sdot);
         ok = __syncthreads_and(ok);
         pa = sdot;
         pb = 0.f;
     } else {
         float m = -INFINITY;
-        if (head_here)
-            m = fmaxf(m, h0);
-        if (tail_here)
-            m = fmaxf(m, t0);
         for (int k = 0; k < nch && ok; ++k) {
             ok = mbar_wait_bounded(smem_addr(&bars[k]), 0);
             const int c1 = (k + 1) * a.chunk_vec < cnt ? (k + 1) * a.chunk_vec : cnt;
@@ -550,6 +548,12 @@ __global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowA
                 }
             }
         }
+        // head and tail (loaded before the chunks landed) last: their load latency
+        // overlaps the chunk waits
+        if (head_here)
+            m = fmaxf(m, h0);
+        if (tail_here)
+            m = fmaxf(m, t0);
         // every chunk has landed once all threads passed the loop above
         ok = __syncthreads_and(ok);
         float d = 0.f;
@@ -886,10 +890,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
             float pa, pb;
             if constexpr (OP == Op::SoftmaxBwd) {
                 float sdot = 0.f;
-                if (head_here)
-                    sdot = fmaf(h0, h1, sdot);
-                if (tail_here)
-                    sdot = fmaf(t0, t1, sdot);
                 for (int64_t kk = 0; kk < nch; ++kk) {
                     const int64_t c0 = kk * CHUNK;
                     const int cn = static_cast<int>((c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0);
@@ -926,25 +926,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                         ph ^= 1u;
                     }
                 }
+                // head and tail, loaded at the row start, are added after the chunks:
+                // their load latency hides behind the chunk waits instead of delaying them
+                if (head_here)
+                    sdot = fmaf(h0, h1, sdot);
+                if (tail_here)
+                    sdot = fmaf(t0, t1, sdot);
                 pa = sdot;
                 pb = 0.f;
             } else {
                 float m = -INFINITY, d = 0.f;
-                {
-                    float hm = -INFINITY;
-                    if (head_here)
-                        hm = h0;
-                    if (tail_here)
-                        hm = fmaxf(hm, t0);
-                    if (hm != -INFINITY) {
-                        m = hm;
-                        const float mL = m * kLog2e;
-                        if (head_here)
-                            d += exp2f(fmaf(h0, kLog2e, -mL));
-                        if (tail_here)
-                            d += exp2f(fmaf(t0, kLog2e, -mL));
-                    }
-                }
                 for (int64_t kk = 0; kk < nch; ++kk) {
                     const int64_t c0 = kk * CHUNK;
                     const int cn = static_cast<int>((c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0);
@@ -1007,6 +998,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                         slot = 0;
                         ph ^= 1u;
                     }
+                }
+                // head and tail, loaded at the row start, are merged after the chunks:
+                // their load latency hides behind the chunk waits instead of delaying them
+                float hm = -INFINITY;
+                if (head_here)
+                    hm = h0;
+                if (tail_here)
+                    hm = fmaxf(hm, t0);
+                if (hm != -INFINITY) {
+                    const float mL = hm * kLog2e;
+                    float hd = 0.f;
+                    if (head_here)
+                        hd += exp2f(fmaf(h0, kLog2e, -mL));
+                    if (tail_here)
+                        hd += exp2f(fmaf(t0, kLog2e, -mL));
+                    md_merge(m, d, hm, hd);
                 }
                 pa = m;
                 pb = d;
