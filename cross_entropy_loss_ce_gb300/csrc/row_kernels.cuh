@@ -1112,7 +1112,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
 #pragma unroll
                             for (int e = 0; e < VEC; ++e)
                                 fy[e] = fy[e] * (fd[e] - r.x);
-                            __stcs(o + vj, E::pack(fy));
+                            o[vj] = E::pack(fy);
                         } else {
                             float f[VEC];
                             E::unpack(raw[v], f);
@@ -1132,7 +1132,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                                             gr[e] = fmaf(f[e], scale, -sub);
                                 }
                             }
-                            __stcs(o + vj, E::pack(gr));
+                            o[vj] = E::pack(gr);
                         }
                     }
                 }
