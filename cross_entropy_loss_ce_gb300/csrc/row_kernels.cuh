@@ -392,7 +392,9 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
 // with up to kMaxChunks bulk copies (one mbarrier each), runs pass 1 as the
 // chunks land, and pass 2 from the staged copy.
 template <Op OP, typename T, int NT>
-__global__ void __launch_bounds__(NT, 1536 / NT) rows_resident_kernel(const RowArgs a)
+// 128-thread CTAs serve short softmax-forward rows: 16 of them per SM
+__global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16 : 1536 / NT)
+    rows_resident_kernel(const RowArgs a)
 {
     using E = Elem<T>;
     using P = Partial<OP>;
