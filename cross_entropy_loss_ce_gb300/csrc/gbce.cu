@@ -31,7 +31,7 @@ constexpr int64_t kRingBytes = 192 * 1024;    // ring capacity per CTA (one CTA 
 constexpr int kRingWarps = 16;                // consumer warps of the ring kernel
 constexpr int kRingVpt1 = 4;                  // vectors per consumer thread and slot, one operand
 constexpr int kRingVpt2 = 2;                  // the same, two operands (softmax backward)
-constexpr int64_t kL2Budget = 56ll << 20;     // bytes of rows between their two reads, all SMs
+constexpr int64_t kL2Budget = 40ll << 20;     // bytes of rows between their two reads, all SMs
 constexpr int64_t kBsrTarget = 32 * 1024;     // block-sparse: bytes per slab stage aimed at
 constexpr int kBsrThreads = 256;              // block-sparse kernels' CTA size
 constexpr int kBsrMaxRows = 64;               // rows per slab (<= kBsrThreads / 4)
