@@ -221,3 +221,26 @@ def test_other_negative_ignore_index():
     assert torch.equal(xd[2].cpu(), x[2])
     keep = [0, 1, 3, 4, 5]
     check_grad(xd[keep], ref["grad"][keep], ref["n"], torch.float32, "ignore_index=-1")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=str)
+@pytest.mark.parametrize("V", [1000, 8000, 100003])   # warp, resident, ring (unaligned rows)
+@pytest.mark.parametrize("offset", [50.0, -150.0, 150.0])
+def test_ce_large_logits(dtype, V, offset):
+    """Logits far from zero, up to a row maximum of about 300 in magnitude (the
+    range in which one rounding of m log2e per partial stays within the fp32
+    tolerance): rows with different offsets, one of them ignored."""
+    require_gpu()
+    M = 6
+    g = torch.Generator().manual_seed(V)
+    x = torch.randn((M, V), generator=g) * 4
+    x += torch.tensor([offset, -offset, 0.5 * offset, offset, 2 * offset, -0.25 * offset])[:, None]
+    t = torch.randint(0, V, (M,), generator=g)
+    t[3] = II
+    xh = x.to(dtype)
+    ref = oracle_ce(xh, t)
+    xd = xh.cuda()
+    loss, status = run_ce(xd, t.cuda())
+    assert status == gbce.OK
+    check_grad(xd, ref["grad"], ref["n"], dtype, f"V={V} offset={offset}")
+    check_loss(loss, oracle.ce_mean(ref["row_loss"], ref["n"]), dtype, f"V={V} offset={offset}")

@@ -81,3 +81,16 @@ def test_softmax_empty():
     x = torch.empty((0, 16), device="cuda")
     assert gbce.softmax_fwd(x).shape == (0, 16)
     assert gbce.softmax_bwd(x, x).shape == (0, 16)
+
+
+@pytest.mark.parametrize("N", [1000, 4096, 16384, 100003])
+@pytest.mark.parametrize("offset", [50.0, -150.0, 150.0])
+def test_softmax_large_inputs(N, offset):
+    """Inputs far from zero (row maxima up to about 300 in magnitude) keep the
+    forward within the fp32 tolerance."""
+    require_gpu()
+    g = torch.Generator().manual_seed(N)
+    x = torch.randn((4, N), generator=g) * 4
+    x += torch.tensor([offset, -offset, 0.5 * offset, 2 * offset])[:, None]
+    ref = oracle.softmax_fwd(host(x))
+    check_softmax(gbce.softmax_fwd(x.cuda()), ref, torch.float32, f"N={N} offset={offset}")
