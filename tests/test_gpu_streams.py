@@ -69,3 +69,51 @@ def test_graph_capture_and_replay(V):
         check_grad(xd, ref["grad"], ref["n"], torch.bfloat16, f"graph replay V={V}")
         check_loss(float(loss.item()), oracle.ce_mean(ref["row_loss"], ref["n"]), torch.bfloat16)
     assert gbce.last_error() == gbce.OK
+
+
+def test_block_sparse_backward_on_two_streams():
+    """Two block-sparse calls in flight on different streams (one in place,
+    one into a separate dx) give the results of the calls made one at a time."""
+    require_gpu()
+    cases = []
+    for name, sizes in (("bsr_f32_causal_2x16x4096_b32", dict(H=2, S=1024)),
+                        ("bsr_bf16_random_4x8x8192_b64", dict(Z=2, H=2, S=2048))):
+        w = workloads.BSR_WORKLOADS[name].with_sizes(**sizes)
+        y, dy, lut, meta = workloads.make_bsr_inputs(w, device="cuda")
+        cases.append((y, dy, lut, meta))
+    args = lambda meta: (meta["n_block_rows"], meta["nblocks"], meta["block"], meta["sizemax"])
+    refs = []
+    for y, dy, lut, meta in cases:  # one at a time
+        refs.append(gbce.softmax_bwd_bsr(y, dy, lut, *args(meta), 0.5, torch.empty_like(dy)))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in cases]
+    outs = []
+    for i, (s, (y, dy, lut, meta)) in enumerate(zip(streams, cases)):
+        with torch.cuda.stream(s):
+            outs.append(gbce.softmax_bwd_bsr(y, dy.clone() if i == 0 else dy, lut, *args(meta), 0.5,
+                                             None if i == 0 else torch.empty_like(dy), stream=s))
+    torch.cuda.synchronize()
+    assert gbce.last_error() == gbce.OK
+    for ref, out in zip(refs, outs):
+        assert torch.equal(ref, out)
+
+
+def test_host_calls_on_two_streams():
+    """Two ce_fwd_bwd_host calls on different streams share the library's copy
+    stream and still give the results of the device call."""
+    require_gpu()
+    cases = [_case(40, 64000, torch.bfloat16, 4), _case(24, 100003, torch.float32, 5)]
+    refs = []
+    for x, t in cases:
+        xd = x.cuda()
+        refs.append((xd, float(gbce.ce_fwd_bwd(xd, t.cuda(), II).item())))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in cases]
+    outs = []
+    for s, (x, t) in zip(streams, cases):
+        with torch.cuda.stream(s):
+            outs.append(gbce.ce_fwd_bwd_host(x.pin_memory(), t.pin_memory(), II, stream=s))
+    torch.cuda.synchronize()
+    assert gbce.last_error() == gbce.OK
+    for (ref_g, ref_l), (grad, loss) in zip(refs, outs):
+        assert torch.equal(grad, ref_g) and float(loss.item()) == ref_l
