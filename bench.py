@@ -346,6 +346,23 @@ def time_ce_e2e(w, x_pinned, t_pinned, steps, ws):
     return total, h2d, 4
 
 
+def host_link_gbs(x_pinned, reps: int = 3) -> float:
+    """Host -> device bandwidth of one plain copy of the pinned logits, measured
+    in the same run (context for the e2e figure: the link bounds it)."""
+    dst = torch.empty(x_pinned.shape, dtype=x_pinned.dtype, device="cuda")
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        start.record()
+        dst.copy_(x_pinned, non_blocking=True)
+        stop.record()
+        torch.cuda.synchronize()
+        best = min(best, start.elapsed_time(stop))
+    del dst
+    return x_pinned.numel() * x_pinned.element_size() / (best / 1e3) / 1e9
+
+
 def time_softmax(steps, warmup, ws, flush, N=16384):
     """Softmax forward, then backward, on the 4096 x N fp32 workload: the
     kernel time of each call from the library's events, L2 flushed before each."""
@@ -488,7 +505,8 @@ def run_gbce(args, ws, rank, local):
         e2e_steps = min(args.steps, 10)
         line["e2e"] = {"value": sum_over_ranks(float(w.M * e2e_steps), ws) / (e2e_ms / 1e3),
                        "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": e2e_ms / e2e_steps}
+                       "ms_per_step": e2e_ms / e2e_steps,
+                       "host_link_h2d_gbs": host_link_gbs(x_pinned)}
         del x_pinned
 
     if rank == 0 and not args.no_cpu_baseline:
