@@ -201,7 +201,7 @@ def replica_throughput(rows_this_rank: float, ms_this_rank: float, ws: int):
 # CPU baseline: the oracle as it stands, on this host's cores
 
 def oracle_rows_per_s(w, x_host: torch.Tensor, t_host: torch.Tensor, block: int = 512,
-                      min_seconds: float = 0.0, max_passes: int = 1):
+                      min_seconds: float = 0.0, max_passes: int = 1, nthreads: int = 0):
     """Time the oracle (loss + full gradient) over the rows of x_host, in blocks;
     repeat the pass (up to max_passes) until min_seconds have elapsed.
     Returns (rows/s, seconds, threads, passes)."""
@@ -210,7 +210,7 @@ def oracle_rows_per_s(w, x_host: torch.Tensor, t_host: torch.Tensor, block: int 
     xa = oracle.host_array(x_host)
     ta = t_host.numpy()
     n, _ = oracle.ce_count(ta, V)
-    nthreads = oracle.default_threads()
+    nthreads = nthreads or oracle.default_threads()
     t0 = time.perf_counter()
     passes = 0
     while passes < max(max_passes, 1):
@@ -222,6 +222,19 @@ def oracle_rows_per_s(w, x_host: torch.Tensor, t_host: torch.Tensor, block: int 
             break
     dt = time.perf_counter() - t0
     return passes * xa.shape[0] / dt, dt, nthreads, passes
+
+
+def single_core_oracle():
+    """The oracle on one host core for the smallest CE workload (all 64 rows)
+    and the 8192 x 32000 bf16 one (its first 1024 rows): rows/s each."""
+    out = {}
+    for name, rows in (("ce_f32_64x1000", 64), ("ce_bf16_8192x32000", 1024)):
+        w = workloads.CE_WORKLOADS[name]
+        x, t = workloads.make_ce_inputs(w.with_rows(rows), "cpu")
+        rps, dt, _, passes = oracle_rows_per_s(w, x, t, min_seconds=0.5, max_passes=50,
+                                               nthreads=1)
+        out[name] = {"rows_per_s": rps, "rows": rows, "passes": passes, "seconds": dt}
+    return out
 
 
 def run_reference(args, ws, rank):
@@ -517,7 +530,8 @@ def run_gbce(args, ws, rank, local):
         line["cpu_baseline"] = {"value": rps, "unit": "rows/s", "cores": cores, "kind": "oracle",
                                 "sample": f"first {sample} rows of {w.name}, {passes} passes: "
                                           f"loss and full gradient in double precision, "
-                                          f"{dt:.1f} s"}
+                                          f"{dt:.1f} s",
+                                "single_core": single_core_oracle()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
