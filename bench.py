@@ -292,7 +292,7 @@ def flush_l2(f: L2Flush):
 
 
 def time_ce(w, xd0, td, steps, warmup, ws, flush):
-    """(step ms summed over K steps, row-kernel ms per launch, loss).
+    """(step ms summed over K steps, row-kernel ms per launch, loss, median step ms).
 
     Every step restores the pristine logits and flushes L2 (untimed), then
     one ce_fwd_bwd call sits between two CUDA events.  The K steps are
@@ -319,7 +319,9 @@ def time_ce(w, xd0, td, steps, warmup, ws, flush):
         gbce.ce_fwd_bwd(xd, td, workloads.IGNORE_INDEX, loss)
         stops[i].record()
     barrier_sync(ws)
-    total = sum(a.elapsed_time(b) for a, b in zip(starts, stops))
+    step_ms = sorted(a.elapsed_time(b) for a, b in zip(starts, stops))
+    total = sum(step_ms)
+    median = (step_ms[(steps - 1) // 2] + step_ms[steps // 2]) / 2
     loss_val = float(loss.item())
     # the row kernel alone (its events split the call, so they are a separate pass)
     kernel_steps = max(steps // 4, 5)
@@ -334,7 +336,7 @@ def time_ce(w, xd0, td, steps, warmup, ws, flush):
     gbce.timing_enable(False)
     if gbce.last_error() != gbce.OK:
         raise RuntimeError("device error flag raised during the timed steps")
-    return total, kms / max(launches, 1), loss_val
+    return total, kms / max(launches, 1), loss_val, median
 
 
 def time_ce_e2e(w, x_pinned, t_pinned, steps, ws):
@@ -466,7 +468,8 @@ def run_gbce(args, ws, rank, local):
     peak, peak_kind = measured_peaks()
 
     with ClockSampler(local) as clocks:
-        total_ms, kavg_ms, loss_val = time_ce(w, xd0, td, args.steps, args.warmup, ws, flush)
+        total_ms, kavg_ms, loss_val, median_ms = time_ce(w, xd0, td, args.steps, args.warmup, ws,
+                                                         flush)
     clk = clocks.summary()
     value, total_ms = replica_throughput(float(w.M * args.steps), total_ms, ws)
     ms_per_step = total_ms / args.steps
@@ -481,7 +484,8 @@ def run_gbce(args, ws, rank, local):
 
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_median": max_over_ranks(median_ms, ws), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
         "config": {"workload": w.name + (f" (first {w.M} rows)" if args.rows else ""), "M": w.M, "V": w.V, "ignore_frac": w.ignore_frac,
