@@ -9,8 +9,8 @@
 // concatenation of row rxm of its blocks.
 //
 // Two kernels, chosen on the host from the longest row (sizemax * block):
-//   bsr_bwd_staged_kernel    one CTA per block-row and batch item, its rows in
-//                            slabs of R.  A slab's piece of every listed block
+//   bsr_bwd_staged_kernel    one CTA (or 2 or 4, each with a share of the rows)
+//                            per block-row and batch item, its rows in slabs of R.  A slab's piece of every listed block
 //                            (R * block contiguous elements per operand) is
 //                            gathered into shared memory with 16-byte
 //                            asynchronous copies, each row's sum(y * dy) is
@@ -47,6 +47,7 @@ struct BsrArgs {
     int sizemax;      // largest valid size of a block-row
     int ids_bytes;    // staged: shared bytes reserved for the block ids (multiple of 16)
     int stage_bytes;  // staged: bytes of one stage (y slab, dy slab; multiple of 16)
+    int log2_split;   // staged: CTAs per block-row and batch item (2^log2_split), each a share of its slabs
     float scale;
 };
 
@@ -130,7 +131,8 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
     __shared__ float s_row[NT / 4];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t task = blockIdx.x;
+    const int64_t task = blockIdx.x >> a.log2_split;
+    const int share = static_cast<int>(blockIdx.x & ((1u << a.log2_split) - 1));
     const int64_t rbm = task % a.nbr;
     const int64_t z = task / a.nbr;
     int32_t *ids = reinterpret_cast<int32_t *>(smem);
@@ -157,7 +159,18 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
         ++lr;
     const int log2_seg = lr + a.log2_block;  // elements of one block's slab
     const int64_t bb = int64_t{1} << (2 * a.log2_block);
-    const int nslab = 1 << (a.log2_block - lr);
+    // this CTA's share of the block-row's slabs: sl0 .. sl0 + nslab - 1
+    const int all_slabs = 1 << (a.log2_block - lr);
+    int nslab, sl0;
+    if (all_slabs >= (1 << a.log2_split)) {
+        nslab = all_slabs >> a.log2_split;
+        sl0 = share * nslab;
+    } else {
+        nslab = share < all_slabs ? 1 : 0;
+        sl0 = share;
+    }
+    if (nslab == 0)
+        return;
     const T *ybase = static_cast<const T *>(a.y) + z * a.ys;
     const T *dybase = static_cast<const T *>(a.dy) + z * a.dys;
     T *xbase = static_cast<T *>(a.dx) + z * a.dxs;
@@ -168,7 +181,7 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
     // Gather slab sl into stage st: piece k = R rows of block ids[k],
     // contiguous in global memory (16-byte asynchronous copies).
     auto issue = [&](int sl, int st) {
-        const int64_t slab_off = int64_t{sl} << log2_seg;
+        const int64_t slab_off = int64_t{sl0 + sl} << log2_seg;
         T *yb = ybuf(st);
         T *db = yb + seg_elems;
         if constexpr (VEC > 1) {
@@ -250,7 +263,7 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
         }
         __syncthreads();
         const float sr = s_row[r];
-        T *xb = xbase + (int64_t{sl} << log2_seg) + (int64_t{r} << a.log2_block);
+        T *xb = xbase + (int64_t{sl0 + sl} << log2_seg) + (int64_t{r} << a.log2_block);
         for (int j = part; j < rv; j += tpr) {
             const int k = j >> log2_bv;
             const int c = j & ((1 << log2_bv) - 1);

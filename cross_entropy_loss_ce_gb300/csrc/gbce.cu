@@ -36,6 +36,8 @@ constexpr int64_t kBsrTarget = 32 * 1024;     // block-sparse: bytes per slab st
 constexpr int kBsrThreads = 256;              // block-sparse kernels' CTA size
 constexpr int kBsrMaxRows = 64;               // rows per slab (<= kBsrThreads / 4)
 constexpr int kBsrStages = 2;                 // slab stages in shared memory
+constexpr int kBsrMaxLog2Split = 2;           // at most 4 CTAs per block-row and batch item
+constexpr int kBsrLog2MinSlabs = 3;           // ... each keeping >= 8 slabs of the longest block-row
 
 size_t elem_size(int dtype) { return dtype == GBCE_F32 ? 4 : 2; }
 
@@ -525,6 +527,7 @@ struct BsrPlan {
     int log2_R;      // staged: rows per slab = 2^log2_R
     int ids_bytes;   // staged: shared bytes for the block ids
     int stage_bytes; // staged: one of the kBsrStages slab stages
+    int log2_split;  // staged: CTAs per block-row and batch item, log2
     int64_t smem;    // staged: dynamic shared memory per CTA
 };
 
@@ -560,6 +563,11 @@ BsrPlan make_bsr_plan(int64_t block, int64_t sizemax, size_t es, bool aligned)
            p.ids_bytes + kBsrStages * stage(l + 1) <= kSliceMax)
         ++l;
     p.log2_R = l;
+    // split long block-rows across CTAs (finer work, a shorter tail), keeping enough slabs
+    // per CTA for the stages to overlap
+    p.log2_split = log2_block - l - kBsrLog2MinSlabs;
+    p.log2_split = p.log2_split < 0 ? 0 : (p.log2_split > kBsrMaxLog2Split ? kBsrMaxLog2Split
+                                                                           : p.log2_split);
     p.stage_bytes = static_cast<int>(stage(l));
     p.smem = p.ids_bytes + kBsrStages * int64_t{p.stage_bytes};
     return p;
@@ -1053,9 +1061,9 @@ extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
                     (dx_zstride * static_cast<int64_t>(es)) % 16 == 0));
     const BsrPlan p = make_bsr_plan(block, sizemax, es, aligned);
     const int log2_block = log2_exact(block);
-    const int per_row_block = p.staged ? 0 : log2_block;
+    const int per_row_block = p.staged ? p.log2_split : log2_block;
     // CTAs = Z * n_block_rows * 2^per_row_block must fit a 1-D grid (staged:
-    // one per block-row and batch item; unstaged: one per row)
+    // 2^log2_split per block-row and batch item; unstaged: one per row)
     const int64_t kGridMax = INT32_MAX;
     if (n_block_rows > (kGridMax >> per_row_block) ||
         Z > (kGridMax >> per_row_block) / n_block_rows)
@@ -1080,6 +1088,7 @@ extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
     a.scale = scale;
 
     a.stage_bytes = p.stage_bytes;
+    a.log2_split = p.log2_split;
     a.max_log2_R = log2_block < log2_exact(kBsrMaxRows) ? log2_block : log2_exact(kBsrMaxRows);
 
     int device = 0;
