@@ -50,7 +50,9 @@ def _close(a, b, rtol, atol, what):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     ok = np.isclose(a, b, rtol=rtol, atol=atol, equal_nan=True)
-    assert ok.all(), f"{what}: max |diff| {np.nanmax(np.abs(a - b))}"
+    diff = np.abs(a - b)
+    worst = np.nanmax(diff) if (~np.isnan(diff)).any() else float("nan")
+    assert ok.all(), f"{what}: max |diff| {worst}"
 
 
 # ---------------------------------------------------------------------------
