@@ -68,9 +68,35 @@ def status_string(code: int) -> str:
     return load_library().gbce_status_string(code).decode()
 
 
-def _stream_handle(stream) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+def _call_device(*named):
+    """The one CUDA device that every tensor of a call lives on.
+
+    ``named`` holds (name, tensor) pairs; None tensors are skipped.  Raises
+    ValueError, before anything is launched, when a tensor is on the host or
+    on another device than the first one: the library works on the current
+    device, so a pointer of another GPU would be handed to the wrong one.
+    """
+    dev = None
+    for name, t in named:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the call's other tensors on {dev}")
+    return dev
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    """The stream of a call on ``device``: the given one (which must belong to
+    that device) or the device's current torch stream."""
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    elif stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+    return ctypes.c_void_p(stream.cuda_stream)
 
 
 def _matrix(t: torch.Tensor, name: str):
@@ -108,9 +134,11 @@ def ce_fwd_bwd(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = 
         loss = torch.empty((), dtype=torch.float32, device=logits.device)
     elif loss.dtype != torch.float32 or loss.numel() != 1 or not loss.is_cuda:
         raise ValueError("loss must be a one-element float32 CUDA tensor")
-    rc = load_library().ce_fwd_bwd(lp, stride, targets.data_ptr(), loss.data_ptr(), M, V,
-                                   int(ignore_index), DTYPES[logits.dtype],
-                                   _stream_handle(stream))
+    dev = _call_device(("logits", logits), ("targets", targets if M else None), ("loss", loss))
+    with torch.cuda.device(dev):
+        rc = load_library().ce_fwd_bwd(lp, stride, targets.data_ptr(), loss.data_ptr(), M, V,
+                                       int(ignore_index), DTYPES[logits.dtype],
+                                       _stream_handle(stream, dev))
     _check(rc, "ce_fwd_bwd")
     return loss
 
@@ -149,11 +177,14 @@ def ce_fwd_bwd_ex(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int
     gs = None
     if grad_scale is not None:
         gs = _device_floats(grad_scale, M if reduction == "none" else 1, dev, "grad_scale")
-    rc = load_library().ce_fwd_bwd_ex(
-        lp, stride, targets.data_ptr(), None if loss is None else loss.data_ptr(),
-        None if row_loss is None else row_loss.data_ptr(), None if gs is None else gs.data_ptr(),
-        M, V, int(ignore_index), DTYPES[logits.dtype], REDUCTIONS[reduction],
-        _stream_handle(stream))
+    dev = _call_device(("logits", logits), ("targets", targets if M else None), ("loss", loss),
+                       ("row_loss", row_loss), ("grad_scale", gs))
+    with torch.cuda.device(dev):
+        rc = load_library().ce_fwd_bwd_ex(
+            lp, stride, targets.data_ptr(), None if loss is None else loss.data_ptr(),
+            None if row_loss is None else row_loss.data_ptr(),
+            None if gs is None else gs.data_ptr(), M, V, int(ignore_index),
+            DTYPES[logits.dtype], REDUCTIONS[reduction], _stream_handle(stream, dev))
     _check(rc, "ce_fwd_bwd_ex")
     return (None if reduction == "none" else loss), row_loss
 
@@ -164,8 +195,10 @@ def scale_rows(x: torch.Tensor, scale, stream=None) -> torch.Tensor:
     xp, stride, M, N = _matrix(x, "x")
     per_row = torch.is_tensor(scale) and scale.numel() == M and M != 1
     sc = _device_floats(scale, M if per_row else 1, x.device, "scale")
-    rc = load_library().scale_rows(xp, stride, M, N, DTYPES[x.dtype], sc.data_ptr(),
-                                   1 if per_row else 0, _stream_handle(stream))
+    dev = _call_device(("x", x), ("scale", sc))
+    with torch.cuda.device(dev):
+        rc = load_library().scale_rows(xp, stride, M, N, DTYPES[x.dtype], sc.data_ptr(),
+                                       1 if per_row else 0, _stream_handle(stream, dev))
     _check(rc, "scale_rows")
     return x
 
@@ -225,7 +258,10 @@ def softmax_fwd(x: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.T
     yp, ys, My, Ny = _matrix(y, "y")
     if (My, Ny) != (M, N) or y.dtype != x.dtype:
         raise ValueError("y must match x in shape and dtype")
-    rc = load_library().softmax_fwd(xp, xs, yp, ys, M, N, DTYPES[x.dtype], _stream_handle(stream))
+    dev = _call_device(("x", x), ("y", y))
+    with torch.cuda.device(dev):
+        rc = load_library().softmax_fwd(xp, xs, yp, ys, M, N, DTYPES[x.dtype],
+                                        _stream_handle(stream, dev))
     _check(rc, "softmax_fwd")
     return y
 
@@ -240,8 +276,10 @@ def softmax_bwd(y: torch.Tensor, dy: torch.Tensor, dx: torch.Tensor = None,
     xp, xs, Mx, Nx = _matrix(dx, "dx")
     if (Md, Nd) != (M, N) or (Mx, Nx) != (M, N) or not (y.dtype == dy.dtype == dx.dtype):
         raise ValueError("y, dy and dx must share shape and dtype")
-    rc = load_library().softmax_bwd(yp, ys, dp, ds, xp, xs, M, N, DTYPES[y.dtype],
-                                    _stream_handle(stream))
+    dev = _call_device(("y", y), ("dy", dy), ("dx", dx))
+    with torch.cuda.device(dev):
+        rc = load_library().softmax_bwd(yp, ys, dp, ds, xp, xs, M, N, DTYPES[y.dtype],
+                                        _stream_handle(stream, dev))
     _check(rc, "softmax_bwd")
     return dx
 
@@ -268,9 +306,12 @@ def softmax_bwd_bsr(y: torch.Tensor, dy: torch.Tensor, lut: torch.Tensor, n_bloc
         raise ValueError("y, dy and dx must hold nblocks * block^2 elements per batch item")
     if lut.dtype != torch.int32 or lut.dim() != 1 or not lut.is_cuda or not lut.is_contiguous():
         raise ValueError("lut must be a contiguous 1-D int32 CUDA tensor")
-    rc = load_library().softmax_bwd_bsr(yp, ys, dp, ds, xp, xs, lut.data_ptr(), lut.numel(),
-                                        n_block_rows, nblocks, block, sizemax, Z, float(scale),
-                                        DTYPES[y.dtype], _stream_handle(stream))
+    dev = _call_device(("y", y), ("dy", dy), ("dx", dx), ("lut", lut))
+    with torch.cuda.device(dev):
+        rc = load_library().softmax_bwd_bsr(yp, ys, dp, ds, xp, xs, lut.data_ptr(), lut.numel(),
+                                            n_block_rows, nblocks, block, sizemax, Z,
+                                            float(scale), DTYPES[y.dtype],
+                                            _stream_handle(stream, dev))
     _check(rc, "softmax_bwd_bsr")
     return dx
 
@@ -298,8 +339,11 @@ def plan(op: str, cols: int, dtype: torch.dtype, same_phase: bool = True):
 
 
 def last_error(stream=None) -> int:
-    """Synchronise the stream and read-and-clear the device error flags."""
-    return load_library().gbce_last_error(_stream_handle(stream))
+    """Synchronise the stream and read-and-clear the error flags of its device
+    (the current device when no stream is given)."""
+    dev = stream.device if stream is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        return load_library().gbce_last_error(_stream_handle(stream, dev))
 
 
 def timing_enable(on: bool = True):
@@ -351,9 +395,11 @@ def ce_fwd_bwd_host(logits_host: torch.Tensor, targets_host: torch.Tensor,
                    ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                    ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
     fn.restype = ctypes.c_int
-    rc = fn(logits_host.data_ptr(), max(hs, V), targets_host.data_ptr(), gp, gs,
-            loss_host.data_ptr(), M, V, int(ignore_index), DTYPES[logits_host.dtype],
-            _stream_handle(stream))
+    dev = _call_device(("grad", grad))
+    with torch.cuda.device(dev):
+        rc = fn(logits_host.data_ptr(), max(hs, V), targets_host.data_ptr(), gp, gs,
+                loss_host.data_ptr(), M, V, int(ignore_index), DTYPES[logits_host.dtype],
+                _stream_handle(stream, dev))
     _check(rc, "ce_fwd_bwd_host")
     return grad, loss_host
 
@@ -367,11 +413,6 @@ def ce_fwd_bwd_noalloc(logits: torch.Tensor, targets: torch.Tensor, ignore_index
     calls that overlap on the GPU must be serialised by the caller.  ``loss``
     is allocated here by torch when not given.
     """
-    lib = load_library()
-    fn = lib.ce_fwd_bwd_noalloc
-    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
-                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
-    fn.restype = ctypes.c_int
     lp, stride, M, V = _matrix(logits, "logits")
     if targets.dtype != torch.int64 or targets.dim() != 1 or targets.shape[0] != M:
         raise ValueError("targets must be int64 of shape [M]")
@@ -381,7 +422,13 @@ def ce_fwd_bwd_noalloc(logits: torch.Tensor, targets: torch.Tensor, ignore_index
         loss = torch.empty((), dtype=torch.float32, device=logits.device)
     elif loss.dtype != torch.float32 or loss.numel() != 1 or not loss.is_cuda:
         raise ValueError("loss must be a one-element float32 CUDA tensor")
-    rc = fn(lp, stride, targets.data_ptr(), loss.data_ptr(), M, V, int(ignore_index),
-            DTYPES[logits.dtype], _stream_handle(stream))
+    dev = _call_device(("logits", logits), ("targets", targets if M else None), ("loss", loss))
+    fn = load_library().ce_fwd_bwd_noalloc
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    with torch.cuda.device(dev):
+        rc = fn(lp, stride, targets.data_ptr(), loss.data_ptr(), M, V, int(ignore_index),
+                DTYPES[logits.dtype], _stream_handle(stream, dev))
     _check(rc, "ce_fwd_bwd_noalloc")
     return loss
