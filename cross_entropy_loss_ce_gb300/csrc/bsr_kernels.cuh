@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
     constexpr int LV = Log2<VEC>::value;
     constexpr int LNT = Log2<NT>::value;
     static_assert(VEC == 1 || VEC * sizeof(T) == 16, "VEC is one element or one 16-byte vector");
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_size;
     __shared__ float s_warp[NT / 32];
     __shared__ float s_row[NT / 4];

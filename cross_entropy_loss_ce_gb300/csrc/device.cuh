@@ -11,6 +11,7 @@
 namespace gbce {
 
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = exp2(x * log2(e))
+constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bulk copy that takes 2 s has failed
 
 // Sticky per-device error flags (read and cleared by gbce_last_error()).
@@ -71,6 +72,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+    return true;
+}
+
+// Wait for phase `parity` of an mbarrier until the %globaltimer value
+// `deadline`: used before a CTA exits, for copies it issued that may still be
+// in flight after a wait gave up.
+__device__ __forceinline__ bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t deadline)
+{
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() > deadline)
             return false;
     }
     return true;
@@ -298,15 +311,40 @@ __device__ __forceinline__ RowGeom row_geom(const T *p, int64_t cols)
 }
 
 // ---------------------------------------------------------------------------
-// (m, d) pairs of the online softmax: m a running maximum, d = sum exp(x - m).
-// Merging two pairs rescales both sums to the larger maximum.  An empty pair
+// exp(x - m) as exp2(x log2(e) - sL), where sL = fl(m log2(e)) is the shift of a
+// partial sum in log2 units.  The product x log2(e) is exact inside the FMA, so
+// the exponent carries one rounding, relative to its own size |x - m| log2(e):
+// the error of a term grows with its distance from the shift, not with the
+// magnitude of the logits.  Every partial keeps its shift in these units and
+// rescales by exp2(sL_a - sL_b) when merging, so numerator and denominator see
+// the same shift and any rounding of m log2(e) cancels in exp(x - m) / sum.
+// sL must be finite (0 for a part that holds only -inf, whose terms are 0).
+__device__ __forceinline__ float exp2_shift(float x, float sL) { return exp2f(fmaf(x, kLog2e, -sL)); }
+
+// The shift of a part whose maximum is m, in log2 units: -inf for an empty
+// part (its sum is 0), else fl(m log2(e)).
+__device__ __forceinline__ float shift_of(float m) { return m * kLog2e; }
+
+// -log p_y = ln D - (x_y log2(e) - SL) ln 2 for the final shift SL and sum D:
+// the difference is one FMA rounding relative to |x_y - m|, so the row loss
+// keeps its relative accuracy whatever the logits' magnitude.
+__device__ __forceinline__ float row_loss_from(float SL, float D, float xy)
+{
+    return logf(D) - fmaf(xy, kLog2e, -SL) * kLn2;
+}
+
+// ---------------------------------------------------------------------------
+// (s, d) pairs of the online softmax: s = fl(m log2(e)) the shift of a running
+// maximum m in log2 units, d = sum exp2(x log2(e) - s).  Merging two pairs
+// rescales both sums to the larger shift by exp2 of the difference of the two
+// stored shifts (exact when they are within a factor of two).  An empty pair
 // is (-inf, 0); two empty pairs merge to an empty pair (no -inf - -inf).
 __device__ __forceinline__ void md_merge(float &m, float &d, float m2, float d2)
 {
     const float mn = fmaxf(m, m2);
     if (mn == -INFINITY)
         return;
-    d = d * exp2f((m - mn) * kLog2e) + d2 * exp2f((m2 - mn) * kLog2e);
+    d = d * exp2f(m - mn) + d2 * exp2f(m2 - mn);
     m = mn;
 }
 

@@ -29,6 +29,10 @@ constexpr int kMaxCluster = 16;
 constexpr int64_t kStreamSlice = 64 * 1024;   // bytes of a row per CTA in the streaming fallback
 constexpr int64_t kRingBytes = 192 * 1024;    // ring capacity per CTA (one CTA per SM)
 constexpr int kRingWarps = 16;                // consumer warps of the ring kernel
+constexpr int kRingWarpsCluster = 15;         // ... when rows are split across a cluster: with
+                                              // the producer, 16 warps (4 per SM sub-partition)
+                                              // may hold 128 registers each, where 17 warps
+                                              // hold 96 and the cluster exchange spilled
 constexpr int kRingVpt1 = 4;                  // vectors per consumer thread and slot, one operand
 constexpr int kRingVpt2 = 2;                  // the same, two operands (softmax backward)
 constexpr int64_t kL2Budget = 40ll << 20;     // bytes of rows between their two reads, all SMs
@@ -124,9 +128,10 @@ Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned,
     p.C = 1;
     while (p.C < kMaxCluster && sms * row_bytes * nbuf / p.C > kL2Budget)
         ++p.C;
-    p.nt = (kRingWarps + 1) * 32;
+    const int ncw = p.C > 1 ? kRingWarpsCluster : kRingWarps;
+    p.nt = (ncw + 1) * 32;
     const int vpt = nbuf == 2 ? kRingVpt2 : kRingVpt1;
-    const int64_t chunk_bytes = static_cast<int64_t>(kRingWarps) * 32 * vpt * 16;
+    const int64_t chunk_bytes = static_cast<int64_t>(ncw) * 32 * vpt * 16;
     p.chunk_vec = static_cast<int>(chunk_bytes / 16);
     p.nslot = static_cast<int>(kRingBytes / (chunk_bytes * nbuf));
     if (p.nslot > kRingMaxSlots)
@@ -144,6 +149,10 @@ Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned,
 
 using KernelFn = void (*)(const RowArgs);
 
+// Failure-path test: the copy CTA 0 of later staged row-kernel launches leaves
+// out (gbce_test_failure_path); -1 for none.
+std::atomic<int> g_drop_copy{-1};
+
 template <Op OP, typename T>
 KernelFn pick_kernel(const Plan &p)
 {
@@ -157,12 +166,16 @@ KernelFn pick_kernel(const Plan &p)
         default: return rows_warp_kernel<OP, T, 16>;
         }
     case Kind::Resident:
-        return p.nt == 128 ? rows_resident_kernel<OP, T, 128> : rows_resident_kernel<OP, T, 256>;
+        if (g_drop_copy.load(std::memory_order_relaxed) >= 0)  // failure-path tests only
+            return p.nt == 128 ? rows_resident_kernel<OP, T, 128, true>
+                               : rows_resident_kernel<OP, T, 256, true>;
+        return p.nt == 128 ? rows_resident_kernel<OP, T, 128, false>
+                           : rows_resident_kernel<OP, T, 256, false>;
     case Kind::Ring: {
         constexpr int vpt = OP == Op::SoftmaxBwd ? kRingVpt2 : kRingVpt1;
         if (p.C > 1)
-            return p.hold ? rows_ring_kernel<OP, T, kRingWarps, vpt, true, true>
-                          : rows_ring_kernel<OP, T, kRingWarps, vpt, true, false>;
+            return p.hold ? rows_ring_kernel<OP, T, kRingWarpsCluster, vpt, true, true>
+                          : rows_ring_kernel<OP, T, kRingWarpsCluster, vpt, true, false>;
         return p.hold ? rows_ring_kernel<OP, T, kRingWarps, vpt, false, true>
                       : rows_ring_kernel<OP, T, kRingWarps, vpt, false, false>;
     }
@@ -355,9 +368,11 @@ cudaError_t resident_clusters(KernelFn fn, const Plan &p, int device, int64_t *o
 // `after_count`: the row kernel follows ce_count_kernel on the stream and may
 // start while it runs (programmatic dependent launch); it waits for it on the
 // device before it reads n.
-cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a, cudaStream_t stream,
+cudaError_t launch_rows(KernelFn fn, const Plan &p, const RowArgs &a_in, cudaStream_t stream,
                         bool after_count = false)
 {
+    RowArgs a = a_in;
+    a.drop_copy = g_drop_copy.load(std::memory_order_relaxed);
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess)
@@ -438,8 +453,10 @@ bool same_phase(const void *a, int64_t sa, const void *b, int64_t sb, size_t esi
 }
 
 // Temporary storage of one cross-entropy call: [0, 4) the non-ignored count
-// n, [kCeScratchHeader, + 4 M) the row losses.
+// n, [4, 8) the call's failure word, [kCeScratchHeader, + 4 M) the row losses.
 constexpr size_t kCeScratchHeader = 256;
+
+unsigned *fail_word(void *scratch) { return reinterpret_cast<unsigned *>(static_cast<char *>(scratch) + 4); }
 
 // The cross-entropy launches on `stream`: the count kernel (n; the reduced
 // loss itself when M == 0), the row kernel, then (mean, sum) the mean kernel,
@@ -452,9 +469,10 @@ cudaError_t launch_ce(void *logits, int64_t stride, const int64_t *targets, floa
                       cudaStream_t stream)
 {
     int *n_ptr = static_cast<int *>(scratch);
+    unsigned *fail = fail_word(scratch);
     if (!row_loss)
         row_loss = reinterpret_cast<float *>(static_cast<char *>(scratch) + kCeScratchHeader);
-    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr, loss,
+    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr, fail, loss,
                                                    reduction);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || M == 0)
@@ -473,6 +491,7 @@ cudaError_t launch_ce(void *logits, int64_t stride, const int64_t *targets, floa
     a.row_loss = row_loss;
     a.reduction = reduction;
     a.grad_scale = grad_scale;
+    a.fail = fail;
     a.C = p.C;
     a.per_vec = p.per_vec;
     a.chunk_vec = p.chunk_vec;
@@ -490,7 +509,8 @@ cudaError_t launch_ce(void *logits, int64_t stride, const int64_t *targets, floa
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, ce_mean_kernel<1024>, static_cast<const float *>(row_loss), M,
-                              static_cast<const int *>(n_ptr), loss, reduction);
+                              static_cast<const int *>(n_ptr), static_cast<const unsigned *>(fail),
+                              loss, reduction);
 }
 
 // ce_fwd_bwd_ex with its temporary storage from the pool.
@@ -663,8 +683,8 @@ cudaError_t launch_ce_host(const void *logits_host, int64_t host_stride,
                             cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess)
         return e;
-    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr, loss_dev,
-                                                   GBCE_MEAN);
+    ce_count_kernel<1024><<<1, 1024, 0, stream>>>(targets, M, V, ignore_index, n_ptr,
+                                                   fail_word(scratch), loss_dev, GBCE_MEAN);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     if (M > 0) {
@@ -716,6 +736,7 @@ cudaError_t launch_ce_host(const void *logits_host, int64_t host_stride,
             a.row_loss = row_loss + r0;
             a.reduction = GBCE_MEAN;
             a.grad_scale = nullptr;
+            a.fail = fail_word(scratch);
             a.C = p.C;
             a.per_vec = p.per_vec;
             a.chunk_vec = p.chunk_vec;
@@ -723,7 +744,8 @@ cudaError_t launch_ce_host(const void *logits_host, int64_t host_stride,
             if ((e = launch_rows(fn, p, a, stream)) != cudaSuccess)
                 return e;
         }
-        ce_mean_kernel<1024><<<1, 1024, 0, stream>>>(row_loss, M, n_ptr, loss_dev, GBCE_MEAN);
+        ce_mean_kernel<1024><<<1, 1024, 0, stream>>>(row_loss, M, n_ptr, fail_word(scratch),
+                                                     loss_dev, GBCE_MEAN);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
@@ -925,6 +947,35 @@ extern "C" const char *gbce_status_string(int status)
     case GBCE_ERR_BAD_TABLE: return "a block-sparse look-up table entry is malformed";
     default: return "unknown status";
     }
+}
+
+extern "C" int gbce_pool_reserved(int device, uint64_t *bytes)
+{
+    if (!bytes)
+        return GBCE_ERR_NULL;
+    if (device < 0 || device >= kMaxDevices)
+        return GBCE_ERR_SIZE;
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lk(g_pool_mu);
+        pool = g_pool[device];
+    }
+    *bytes = 0;
+    if (!pool)
+        return GBCE_OK;
+    uint64_t v = 0;  // the attribute is a 64-bit unsigned value
+    cudaError_t e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &v);
+    if (e == cudaSuccess)
+        *bytes = static_cast<uint64_t>(v);
+    return map_error(e);
+}
+
+extern "C" int gbce_test_failure_path(int64_t drop_copy)
+{
+    if (drop_copy > INT32_MAX)
+        return GBCE_ERR_SIZE;
+    g_drop_copy.store(drop_copy < 0 ? -1 : static_cast<int>(drop_copy));
+    return GBCE_OK;
 }
 
 extern "C" int gbce_timing_enable(int on)

@@ -52,6 +52,11 @@ struct RowArgs {
     float *row_loss;    // [M]
     int reduction;      // kReduceMean / kReduceSum / kReduceNone
     const float *grad_scale;  // NULL (1), one value, or one per row (kReduceNone)
+    unsigned *fail;     // this call's failure word, cleared by ce_count_kernel (NULL: none)
+    // Failure-path test (gbce_test_failure_path): the bulk copy, counted from 0,
+    // that CTA 0 of the launch leaves out; -1 (always, outside such tests) for none.
+    // The copy's barrier phase then never completes and the waits for it give up.
+    int drop_copy;
     // launch plan
     int C;          // CTAs per row (cluster size; ring and streaming kernels)
     int per_vec;    // resident: 16-byte vectors staged per operand
@@ -61,6 +66,17 @@ struct RowArgs {
 
 // Sticky error flags of this device (kFlag* bits); defined once per library.
 __device__ unsigned int g_flags = 0;
+
+// A bounded wait of this call gave up: the device flag, and for the
+// cross-entropy the call's own failure word, which makes its reduced loss NaN.
+// A cross-entropy caller has passed wait_prerequisite_grid() (the count kernel
+// clears the word).
+__device__ __forceinline__ void raise_timeout(unsigned *fail)
+{
+    atomicOr(&g_flags, kFlagTimeout);
+    if (fail)
+        atomicOr(fail, 1u);
+}
 
 template <Op OP>
 struct Partial {
@@ -95,6 +111,13 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads)
 
 // Wait for the kernel this one depends on (launched before it with
 // programmatic stream serialisation) to complete and publish its writes.
+//
+// ce_row_exit_order: every CTA of a cross-entropy row kernel executes this
+// before it exits, also on the early exits of ignored rows and bad targets
+// that read no n.  The mean kernel waits only for the row kernel; because no
+// row-kernel CTA can finish before the count kernel has, the row kernel's
+// completion implies the count kernel's, and the mean kernel reads this
+// call's n even when every row was ignored.
 __device__ __forceinline__ void wait_prerequisite_grid()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -216,6 +239,7 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
                 E::store(out + g.tail_start + lane, 0.f);
             if (lane == 0)
                 a.row_loss[row] = 0.f;
+            wait_prerequisite_grid();  // see ce_row_exit_order
             return;
         }
         if (y < 0 || y >= a.cols) {
@@ -223,6 +247,7 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
                 a.row_loss[row] = __int_as_float(0x7fc00000);
                 atomicOr(&g_flags, kFlagBadTarget);
             }
+            wait_prerequisite_grid();
             return;
         }
     }
@@ -313,7 +338,8 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        const float ML = (m == -INFINITY) ? 0.f : m * kLog2e;
+        // the row's shift in log2 units (0 for an all -inf row, whose terms are 0)
+        const float sL = (m == -INFINITY) ? 0.f : shift_of(m);
         float d = 0.f;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
@@ -322,13 +348,13 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
                 E::unpack(r0[v], f);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    d += exp2f(fmaf(f[e], kLog2e, -ML));
+                    d += exp2_shift(f[e], sL);
             }
         }
         if (head_here)
-            d += exp2f(fmaf(h0, kLog2e, -ML));
+            d += exp2_shift(h0, sL);
         if (tail_here)
-            d += exp2f(fmaf(t0, kLog2e, -ML));
+            d += exp2_shift(t0, sL);
         d = warp_sum(d);
 
         float scale, sub = 0.f;
@@ -349,14 +375,14 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
                 float gr[VEC];
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    gr[e] = exp2f(fmaf(f[e], kLog2e, -ML)) * scale;
+                    gr[e] = exp2_shift(f[e], sL) * scale;
                 if constexpr (OP == Op::CE) {
                     const int64_t rel = ycol - static_cast<int64_t>(j) * VEC;
                     if (rel >= 0 && rel < VEC) {  // the target column: (p_y - 1) / n
 #pragma unroll
                         for (int e = 0; e < VEC; ++e)
                             if (e == rel) {
-                                gr[e] = fmaf(exp2f(fmaf(f[e], kLog2e, -ML)), scale, -sub);
+                                gr[e] = fmaf(exp2_shift(f[e], sL), scale, -sub);
                                 xy = f[e];
                             }
                     }
@@ -365,13 +391,13 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
             }
         }
         if (head_here) {
-            const float ex = exp2f(fmaf(h0, kLog2e, -ML));
+            const float ex = exp2_shift(h0, sL);
             E::store(out + lane, (OP == Op::CE && y == lane) ? fmaf(ex, scale, -sub) : ex * scale);
             if (OP == Op::CE && y == lane)
                 xy = h0;
         }
         if (tail_here) {
-            const float ex = exp2f(fmaf(t0, kLog2e, -ML));
+            const float ex = exp2_shift(t0, sL);
             const bool at_y = OP == Op::CE && y == g.tail_start + lane;
             E::store(out + g.tail_start + lane, at_y ? fmaf(ex, scale, -sub) : ex * scale);
             if (at_y)
@@ -381,7 +407,7 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
             // exactly one lane holds the target logit; the others contribute 0
             xy = warp_sum(xy);
             if (lane == 0)
-                a.row_loss[row] = m + logf(d) - xy;
+                a.row_loss[row] = row_loss_from(sL, d, xy);
         }
     }
 }
@@ -391,9 +417,18 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) rows_warp_kernel(const R
 // per row in all): one CTA per row, three CTAs per SM.  The CTA stages its row
 // with up to kMaxChunks bulk copies (one mbarrier each), runs pass 1 as the
 // chunks land, and pass 2 from the staged copy.
-template <Op OP, typename T, int NT>
-// 128-thread CTAs serve short softmax-forward rows: 16 of them per SM
-__global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16 : 1536 / NT)
+// Residency: 128-thread CTAs serve short softmax-forward rows, 16 of them per
+// SM; otherwise 1536 threads per SM, except the fp32 softmax backward with
+// 1280 (48 registers: at 40 it spilled 28 bytes; measured on 4096 x 4096 fp32,
+// 1280 and 1536 threads run alike, while 1024 threads, 64 registers, ran 8%
+// slower).
+// DROP: the instance for failure-path tests only (a.drop_copy may name a copy
+// CTA 0 leaves out); the others carry no trace of the test (the check in the
+// issue loop alone cost 4% on 4096 x 4096 fp32 rows).
+template <Op OP, typename T, int NT, bool DROP>
+__global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16
+                                      : ((OP == Op::SoftmaxBwd && sizeof(T) == 4) ? 1280 / NT
+                                                                                 : 1536 / NT))
     rows_resident_kernel(const RowArgs a)
 {
     using E = Elem<T>;
@@ -441,6 +476,7 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16 :
                 E::store(out + g.tail_start + tid, 0.f);
             if (tid == 0)
                 a.row_loss[row] = 0.f;
+            wait_prerequisite_grid();  // see ce_row_exit_order
             return;
         }
         if (y < 0 || y >= a.cols) {
@@ -449,6 +485,7 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16 :
                 a.row_loss[row] = __int_as_float(0x7fc00000);
                 atomicOr(&g_flags, kFlagBadTarget);
             }
+            wait_prerequisite_grid();
             return;
         }
     }
@@ -465,7 +502,10 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16 :
     __syncthreads();
     if (tid == 0) {
         const uint64_t pol = policy_evict_first();
+        const int drop = (DROP && blockIdx.x == 0) ? a.drop_copy : -1;
         for (int k = 0; k < nch; ++k) {
+            if (DROP && k == drop)
+                continue;  // failure-path test: this chunk never lands
             const int c0 = k * a.chunk_vec;
             const int c1 = c0 + a.chunk_vec < cnt ? c0 + a.chunk_vec : cnt;
             const uint32_t bytes = static_cast<uint32_t>(c1 - c0) * 16u;
@@ -560,20 +600,21 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16 :
         ok = __syncthreads_and(ok);
         float d = 0.f;
         if (ok) {
-            const float mL = (m == -INFINITY) ? 0.f : m * kLog2e;
+            // this thread's shift in log2 units (0 if it saw only -inf: its terms are 0)
+            const float sL = (m == -INFINITY) ? 0.f : shift_of(m);
             for (int j = tid; j < cnt; j += NT) {
                 float f[VEC];
                 E::unpack(ld_shared_v4(buf0 + j * 16u), f);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    d += exp2f(fmaf(f[e], kLog2e, -mL));
+                    d += exp2_shift(f[e], sL);
             }
             if (head_here)
-                d += exp2f(fmaf(h0, kLog2e, -mL));
+                d += exp2_shift(h0, sL);
             if (tail_here)
-                d += exp2f(fmaf(t0, kLog2e, -mL));
+                d += exp2_shift(t0, sL);
         }
-        pa = m;
+        pa = shift_of(m);  // (shift, sum) partial; (-inf, 0) when empty
         pb = d;
     }
 
@@ -611,8 +652,7 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16 :
             if (tail_here)
                 E::store(out + g.tail_start + tid, t0 * (t1 - sdot));
         } else {
-            const float M = r.x, D = r.y;
-            const float ML = M * kLog2e;
+            const float SL = r.x, D = r.y;  // the row's shift (log2 units) and sum
             float scale, sub = 0.f;
             if constexpr (OP == Op::CE) {
                 wait_prerequisite_grid();  // n comes from the count kernel
@@ -626,7 +666,7 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16 :
                 E::unpack(ld_shared_v4(buf0 + j * 16u), f);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    f[e] = exp2f(fmaf(f[e], kLog2e, -ML));
+                    f[e] = exp2_shift(f[e], SL);
                 float gr[VEC];
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
@@ -643,28 +683,33 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16 :
                 __stcs(o + j, E::pack(gr));
             }
             if (head_here) {
-                const float ex = exp2f(fmaf(h0, kLog2e, -ML));
+                const float ex = exp2_shift(h0, SL);
                 E::store(out + tid, (OP == Op::CE && y == tid) ? fmaf(ex, scale, -sub) : ex * scale);
             }
             if (tail_here) {
-                const float ex = exp2f(fmaf(t0, kLog2e, -ML));
+                const float ex = exp2_shift(t0, SL);
                 E::store(out + g.tail_start + tid,
                          (OP == Op::CE && y == g.tail_start + tid) ? fmaf(ex, scale, -sub)
                                                                     : ex * scale);
             }
             if constexpr (OP == Op::CE) {
                 if (tid == 0)
-                    a.row_loss[row] = M + logf(D) - xy;
+                    a.row_loss[row] = row_loss_from(SL, D, xy);
             }
         }
     } else {
         if (tid == 0) {
-            atomicOr(&g_flags, kFlagTimeout);
-            if constexpr (OP == Op::CE)
+            if constexpr (OP == Op::CE) {
+                wait_prerequisite_grid();  // the count kernel has cleared the failure word
                 a.row_loss[row] = __int_as_float(0x7fc00000);
-            // give copies still in flight a bounded chance to land before exit
+            }
+            raise_timeout(a.fail);
+            // copies still in flight land before the CTA exits (a fixed budget)
+            const int drop = (DROP && blockIdx.x == 0) ? a.drop_copy : -1;
+            const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
             for (int k = 0; k < nch; ++k)
-                mbar_wait_bounded(smem_addr(&bars[k]), 0);
+                if (k != drop)
+                    mbar_wait_until(smem_addr(&bars[k]), 0, deadline);
         }
     }
 }
@@ -731,14 +776,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
     __shared__ __align__(8) uint64_t xbar[2];  // cluster exchange, by live-row parity
     __shared__ __align__(16) float4 xslot[2][kRingMaxCluster];
     __shared__ float2 red[NCW];
+    __shared__ int wbad[NCW];  // a consumer warp whose wait gave up (this row or before)
     __shared__ float4 fin;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int C = CLUSTER ? a.C : 1;
     const int rank = CLUSTER ? static_cast<int>(cluster_rank()) : 0;
-    const int64_t cid = blockIdx.x / C;
-    const int64_t G = gridDim.x / C;
+    // 32-bit row and vector indices throughout (rows < 2^27 and columns < 2^31
+    // are checked on the host); only the row base addresses are 64-bit
+    const int cid = static_cast<int>(blockIdx.x) / C;
+    const int G = static_cast<int>(gridDim.x) / C;
+    const int M = static_cast<int>(a.M);
     const int nslot = a.nslot;
     const uint32_t ring = smem_addr(smem);
 
@@ -763,10 +812,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
             const uint64_t keep = policy_evict_last(), stream = policy_evict_first();
             uint32_t slot = 0, ph = 0;
             bool ok = true;
-            int64_t ynext = (OP == Op::CE && cid < a.M) ? a.targets[cid] : 0;
-            for (int64_t row = cid; row < a.M && ok; row += G) {
+            // slots filled at least once, and the phase of each slot's last fill
+            uint32_t filled = 0, fill_ph = 0;
+            uint32_t issued = 0;  // copies issued so far, the left-out one included
+            const int drop = blockIdx.x == 0 ? a.drop_copy : -1;
+            int64_t ynext = (OP == Op::CE && cid < M) ? a.targets[cid] : 0;
+            for (int row = cid; row < M && ok; row += G) {
                 const int64_t y = ynext;
-                if (OP == Op::CE && row + G < a.M)
+                if (OP == Op::CE && row + G < M)
                     ynext = a.targets[row + G];
                 if (!row_is_live<OP>(a, y))
                     continue;  // ignored or invalid target: nothing to read
@@ -775,19 +828,20 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                 if constexpr (NBUF == 2)
                     in1 = static_cast<const T *>(a.in1) + row * a.s1;
                 const RowGeom g = row_geom(in0, a.cols);
-                const int64_t per = (g.nvec + C - 1) / C;
-                const int64_t v0 = rank * per;
-                const int64_t cnt = v0 < g.nvec ? (v0 + per < g.nvec ? per : g.nvec - v0) : 0;
-                const int64_t body = g.head + v0 * VEC;
-                const int64_t nch = (cnt + CHUNK - 1) / CHUNK;
+                const int nvec = static_cast<int>(g.nvec);
+                const int per = (nvec + C - 1) / C;
+                const int v0 = rank * per;
+                const int cnt = v0 < nvec ? (v0 + per < nvec ? per : nvec - v0) : 0;
+                const int body = g.head + v0 * VEC;
+                const int nch = (cnt + CHUNK - 1) / CHUNK;
                 if (HOLD && 2 * nch > nslot)
                     continue;  // outside the launch's bound: the consumers skip it too
                 // a held slice is loaded once; otherwise the row is streamed twice
                 constexpr int passes = HOLD ? 1 : 2;
                 for (int pass = 0; pass < passes && ok; ++pass) {
-                    for (int64_t kk = 0; kk < nch; ++kk) {
-                        const int64_t c0 = kk * CHUNK;
-                        const int64_t c1 = c0 + CHUNK < cnt ? c0 + CHUNK : cnt;
+                    for (int kk = 0; kk < nch; ++kk) {
+                        const int c0 = kk * CHUNK;
+                        const int c1 = c0 + CHUNK < cnt ? c0 + CHUNK : cnt;
                         const uint32_t bytes = static_cast<uint32_t>(c1 - c0) * 16u;
                         if (!mbar_wait_bounded(smem_addr(&empty[slot]), ph ^ 1u)) {
                             ok = false;
@@ -796,11 +850,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                         }
                         const uint32_t fb = smem_addr(&full[slot]);
                         const uint32_t dst = ring + slot * kSlotBytes;
-                        mbar_arrive_expect_tx(fb, bytes * NBUF);
-                        bulk_load(dst, in0 + body + c0 * VEC, bytes, fb, pass == 0 ? keep : stream);
-                        if constexpr (NBUF == 2)
-                            bulk_load(dst + kChunkBytes, in1 + body + c0 * VEC, bytes, fb,
+                        if (drop >= 0 && issued == static_cast<uint32_t>(drop)) {
+                            // failure-path test: this fill is left out, its phase never completes
+                        } else {
+                            mbar_arrive_expect_tx(fb, bytes * NBUF);
+                            bulk_load(dst, in0 + body + c0 * VEC, bytes, fb,
                                       pass == 0 ? keep : stream);
+                            if constexpr (NBUF == 2)
+                                bulk_load(dst + kChunkBytes, in1 + body + c0 * VEC, bytes, fb,
+                                          pass == 0 ? keep : stream);
+                            filled |= 1u << slot;
+                            fill_ph = (fill_ph & ~(1u << slot)) | (ph << slot);
+                        }
+                        ++issued;
                         if (++slot == static_cast<uint32_t>(nslot)) {
                             slot = 0;
                             ph ^= 1u;
@@ -808,6 +870,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                     }
                 }
             }
+            // Every copy issued here lands before the CTA may exit (consumers
+            // that gave up no longer wait for them): the last fill of each slot
+            // completes the phase recorded for it (a left-out fill records
+            // nothing; the slot's earlier fill, if any, has long landed).  A
+            // fixed budget bounds the whole drain.
+            const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+            for (int s = 0; s < nslot; ++s)
+                if ((filled >> s) & 1u)
+                    mbar_wait_until(smem_addr(&full[s]), (fill_ph >> s) & 1u, deadline);
         }
     } else {
         // ------------------------------------------------------------ consumers
@@ -821,10 +892,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
             wait_prerequisite_grid();  // n comes from the count kernel
         }
         const float nf = OP == Op::CE ? static_cast<float>(*a.n_ptr) : 1.f;
-        int64_t ynext = (OP == Op::CE && cid < a.M) ? a.targets[cid] : 0;
-        for (int64_t row = cid; row < a.M; row += G) {
+        int64_t ynext = (OP == Op::CE && cid < M) ? a.targets[cid] : 0;
+        for (int row = cid; row < M; row += G) {
             const int64_t y = ynext;  // loaded one row ahead
-            if (OP == Op::CE && row + G < a.M)
+            if (OP == Op::CE && row + G < M)
                 ynext = a.targets[row + G];
             const T *in0 = static_cast<const T *>(a.in0) + row * a.s0;
             const T *in1 = nullptr;
@@ -832,22 +903,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                 in1 = static_cast<const T *>(a.in1) + row * a.s1;
             T *out = static_cast<T *>(a.out) + row * a.so;
             const RowGeom g = row_geom(in0, a.cols);
-            const int64_t per = (g.nvec + C - 1) / C;
-            const int64_t v0 = rank * per;
-            const int64_t cnt = v0 < g.nvec ? (v0 + per < g.nvec ? per : g.nvec - v0) : 0;
-            const int64_t body = g.head + v0 * VEC;
+            const int nvec = static_cast<int>(g.nvec);
+            const int tail_start = static_cast<int>(g.tail_start);
+            const int per = (nvec + C - 1) / C;
+            const int v0 = rank * per;
+            const int cnt = v0 < nvec ? (v0 + per < nvec ? per : nvec - v0) : 0;
+            const int body = g.head + v0 * VEC;
             const bool head_here = rank == 0 && tid < g.head;
             const bool tail_here = rank == C - 1 && tid < g.tail;
             uint4 *o = reinterpret_cast<uint4 *>(out + body);
             if constexpr (OP == Op::CE) {
                 if (y == a.ignore_index) {
                     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                    for (int64_t j = tid; j < cnt; j += NC)
+                    for (int j = tid; j < cnt; j += NC)
                         __stcs(o + j, z);
                     if (head_here)
                         E::store(out + tid, 0.f);
                     if (tail_here)
-                        E::store(out + g.tail_start + tid, 0.f);
+                        E::store(out + tail_start + tid, 0.f);
                     if (rank == 0 && tid == 0)
                         a.row_loss[row] = 0.f;
                     continue;
@@ -860,7 +933,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                     continue;
                 }
             }
-            const int64_t nch = (cnt + CHUNK - 1) / CHUNK;
+            const int nch = (cnt + CHUNK - 1) / CHUNK;
             if (HOLD && 2 * nch > nslot) {  // cannot happen for a valid plan: flag, skip
                 if (tid == 0) {
                     atomicOr(&g_flags, kFlagTimeout);
@@ -878,9 +951,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                     h1 = E::load(in1 + tid);
             }
             if (tail_here) {
-                t0 = E::load(in0 + g.tail_start + tid);
+                t0 = E::load(in0 + tail_start + tid);
                 if constexpr (NBUF == 2)
-                    t1 = E::load(in1 + g.tail_start + tid);
+                    t1 = E::load(in1 + tail_start + tid);
             }
             float xy = 0.f;
             if constexpr (OP == Op::CE) {
@@ -892,9 +965,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
             float pa, pb;
             if constexpr (OP == Op::SoftmaxBwd) {
                 float sdot = 0.f;
-                for (int64_t kk = 0; kk < nch; ++kk) {
-                    const int64_t c0 = kk * CHUNK;
-                    const int cn = static_cast<int>((c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0);
+                for (int kk = 0; kk < nch; ++kk) {
+                    const int c0 = kk * CHUNK;
+                    const int cn = (c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0;
                     if (ok)
                         ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[slot]), ph));
                     if (ok) {
@@ -937,10 +1010,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                 pa = sdot;
                 pb = 0.f;
             } else {
-                float m = -INFINITY, d = 0.f;
-                for (int64_t kk = 0; kk < nch; ++kk) {
-                    const int64_t c0 = kk * CHUNK;
-                    const int cn = static_cast<int>((c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0);
+                float m = -INFINITY, d = 0.f;  // running shift (log2 units) and sum
+                for (int kk = 0; kk < nch; ++kk) {
+                    const int c0 = kk * CHUNK;
+                    const int cn = (c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0;
                     if (ok)
                         ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[slot]), ph));
                     if (ok) {
@@ -975,9 +1048,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                                 }
                             }
                         }
-                        const float mn = fmaxf(m, cm);
+                        // the running shift in log2 units: fl(x log2 e) is monotonic,
+                        // so the shift of the larger maximum is the larger shift
+                        const float mn = fmaxf(m, shift_of(cm));
                         if (mn != -INFINITY) {
-                            const float mL = mn * kLog2e;
                             float s = 0.f;
 #pragma unroll
                             for (int v = 0; v < VPT; ++v) {
@@ -986,10 +1060,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                                     E::unpack(raw[v], f);
 #pragma unroll
                                     for (int e = 0; e < VEC; ++e)
-                                        s += exp2f(fmaf(f[e], kLog2e, -mL));
+                                        s += exp2_shift(f[e], mn);
                                 }
                             }
-                            d = d * exp2f((m - mn) * kLog2e) + s;
+                            d = d * exp2f(m - mn) + s;
                             m = mn;
                         }
                     }
@@ -1009,30 +1083,34 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                 if (tail_here)
                     hm = fmaxf(hm, t0);
                 if (hm != -INFINITY) {
-                    const float mL = hm * kLog2e;
+                    const float hL = shift_of(hm);
                     float hd = 0.f;
                     if (head_here)
-                        hd += exp2f(fmaf(h0, kLog2e, -mL));
+                        hd += exp2_shift(h0, hL);
                     if (tail_here)
-                        hd += exp2f(fmaf(t0, kLog2e, -mL));
-                    md_merge(m, d, hm, hd);
+                        hd += exp2_shift(t0, hL);
+                    md_merge(m, d, hL, hd);
                 }
                 pa = m;
                 pb = d;
             }
 
-            // ---- merge across the consumer warps
+            // ---- merge across the consumer warps; a row is good only if every
+            // warp's waits succeeded up to here (a warp that gave up stays out)
             P::warp_reduce(pa, pb);
-            if (lane == 0)
+            if (lane == 0) {
                 red[warp] = make_float2(pa, pb);
+                wbad[warp] = ok ? 0 : 1;
+            }
             named_barrier_sync(1, NC);
             if (warp == 0) {
                 const float2 e = P::empty();
                 pa = lane < NCW ? red[lane].x : e.x;
                 pb = lane < NCW ? red[lane].y : e.y;
+                const bool bad = __any_sync(0xffffffffu, lane < NCW && wbad[lane] != 0);
                 P::warp_reduce(pa, pb);
                 if (lane == 0)
-                    fin = make_float4(pa, pb, ok ? 0.f : 1.f, 0.f);
+                    fin = make_float4(pa, pb, bad ? 1.f : 0.f, 0.f);
             }
             named_barrier_sync(1, NC);
             float4 r = fin;
@@ -1070,23 +1148,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
 
             // ---- pass 2: the slice again (the same slots when held, else a
             // second read that L2 serves), chunks in order
-            float scale = 0.f, sub = 0.f, ML = 0.f;
+            float scale = 0.f, sub = 0.f;
             if constexpr (OP != Op::SoftmaxBwd) {
-                ML = r.x * kLog2e;
                 if constexpr (OP == Op::CE)
                     ce_row_factor(a, row, r.y, nf, scale, sub);
                 else
                     scale = 1.f / r.y;
             }
             const bool all_ok = r.z == 0.f;
-            const int64_t ycol = y - body;
+            const int ycol = static_cast<int>(y) - body;  // y is in [0, cols) here
             if (hold) {  // revisit the slots pass 1 read
                 slot = slot0;
                 ph = ph0;
             }
-            for (int64_t kk = 0; kk < nch; ++kk) {
-                const int64_t c0 = kk * CHUNK;
-                const int cn = static_cast<int>((c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0);
+            for (int kk = 0; kk < nch; ++kk) {
+                const int c0 = kk * CHUNK;
+                const int cn = (c0 + CHUNK < cnt ? c0 + CHUNK : cnt) - c0;
                 if (ok && !hold)
                     ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[slot]), ph));
                 if (ok && all_ok) {
@@ -1106,7 +1183,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                         const int j = tid + v * NC;
                         if (j >= cn)
                             continue;
-                        const int64_t vj = c0 + j;  // vector index within the slice
+                        const int vj = c0 + j;  // vector index within the slice
                         if constexpr (OP == Op::SoftmaxBwd) {
                             float fy[VEC], fd[VEC];
                             E::unpack(raw[v], fy);
@@ -1120,13 +1197,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                             E::unpack(raw[v], f);
 #pragma unroll
                             for (int e = 0; e < VEC; ++e)
-                                f[e] = exp2f(fmaf(f[e], kLog2e, -ML));
+                                f[e] = exp2_shift(f[e], r.x);
                             float gr[VEC];
 #pragma unroll
                             for (int e = 0; e < VEC; ++e)
                                 gr[e] = f[e] * scale;
                             if constexpr (OP == Op::CE) {
-                                const int64_t rel = ycol - vj * VEC;
+                                const int rel = ycol - vj * VEC;
                                 if (rel >= 0 && rel < VEC) {  // the target column: (p_y - 1) / n
 #pragma unroll
                                     for (int e = 0; e < VEC; ++e)
@@ -1151,36 +1228,41 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                     if (head_here)
                         E::store(out + tid, h0 * (h1 - r.x));
                     if (tail_here)
-                        E::store(out + g.tail_start + tid, t0 * (t1 - r.x));
+                        E::store(out + tail_start + tid, t0 * (t1 - r.x));
                 } else {
                     if (head_here) {
-                        const float ex = exp2f(fmaf(h0, kLog2e, -ML));
+                        const float ex = exp2_shift(h0, r.x);
                         E::store(out + tid,
                                  (OP == Op::CE && y == tid) ? fmaf(ex, scale, -sub) : ex * scale);
                     }
                     if (tail_here) {
-                        const float ex = exp2f(fmaf(t0, kLog2e, -ML));
-                        E::store(out + g.tail_start + tid,
-                                 (OP == Op::CE && y == g.tail_start + tid) ? fmaf(ex, scale, -sub)
+                        const float ex = exp2_shift(t0, r.x);
+                        E::store(out + tail_start + tid,
+                                 (OP == Op::CE && y == tail_start + tid) ? fmaf(ex, scale, -sub)
                                                                             : ex * scale);
                     }
                     if constexpr (OP == Op::CE) {
                         if (rank == 0 && tid == 0)
-                            a.row_loss[row] = r.x + logf(r.y) - xy;
+                            a.row_loss[row] = row_loss_from(r.x, r.y, xy);
                     }
                 }
             } else if (tid == 0) {
-                atomicOr(&g_flags, kFlagTimeout);
+                raise_timeout(a.fail);
                 if constexpr (OP == Op::CE) {
                     if (rank == 0)
                         a.row_loss[row] = __int_as_float(0x7fc00000);
                 }
             }
         }
-        if (!ok && lane == 0) {
-            // a wait gave up: linger (bounded) so copies still in flight land before exit
-            const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < kWaitLimitNs / 10) {
+        if (!ok && lane == 0)  // this warp gave up (perhaps in a last pass 2 no row vote saw)
+            raise_timeout(a.fail);
+        if constexpr (CLUSTER) {
+            // a CTA that gave up stopped waiting for its peers' partials: let the
+            // last one of each exchange barrier land before the CTA may exit
+            if (tid == 0 && live > 0) {
+                const uint64_t deadline = globaltimer_ns() + kWaitLimitNs;
+                for (int pi = 0; pi < 2 && pi < live; ++pi)
+                    mbar_wait_until(smem_addr(&xbar[pi]), ((xph >> pi) & 1u) ^ 1u, deadline);
             }
         }
     }
@@ -1226,6 +1308,7 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
                 E::store(out + i, 0.f);
             if (rank == 0 && tid == 0)
                 a.row_loss[row] = 0.f;
+            wait_prerequisite_grid();  // see ce_row_exit_order
             return;
         }
         if (y < 0 || y >= a.cols) {
@@ -1233,6 +1316,7 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
                 a.row_loss[row] = __int_as_float(0x7fc00000);
                 atomicOr(&g_flags, kFlagBadTarget);
             }
+            wait_prerequisite_grid();
             return;
         }
     }
@@ -1252,11 +1336,11 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
         float m = -INFINITY;
         for (int64_t i = e0 + tid; i < e1; i += NT)
             m = fmaxf(m, E::load(in0 + i));
-        const float mL = (m == -INFINITY) ? 0.f : m * kLog2e;
+        const float sL = (m == -INFINITY) ? 0.f : shift_of(m);  // all -inf: every term 0
         float d = 0.f;
         for (int64_t i = e0 + tid; i < e1; i += NT)
-            d += exp2f(fmaf(E::load(in0 + i), kLog2e, -mL));
-        pa = m;
+            d += exp2_shift(E::load(in0 + i), sL);
+        pa = shift_of(m);  // (shift, sum) partial; (-inf, 0) when empty
         pb = d;
     }
     P::warp_reduce(pa, pb);
@@ -1301,7 +1385,6 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
             E::store(out + i, yv * (E::load(in1 + i) - r.x));
         }
     } else {
-        const float ML = r.x * kLog2e;
         float scale, sub = 0.f;
         if constexpr (OP == Op::CE) {
             wait_prerequisite_grid();  // n comes from the count kernel
@@ -1312,12 +1395,12 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
         // Read every element before this thread overwrites it (in place for CE);
         // each element is read and written by the same thread only.
         for (int64_t i = e0 + tid; i < e1; i += NT) {
-            const float ex = exp2f(fmaf(E::load(in0 + i), kLog2e, -ML));
+            const float ex = exp2_shift(E::load(in0 + i), r.x);
             E::store(out + i, (OP == Op::CE && i == y) ? fmaf(ex, scale, -sub) : ex * scale);
         }
         if constexpr (OP == Op::CE) {
             if (rank == 0 && tid == 0)
-                a.row_loss[row] = r.x + logf(r.y) - xy;
+                a.row_loss[row] = row_loss_from(r.x, r.y, xy);
         }
     }
     if (C > 1)
@@ -1332,7 +1415,7 @@ __global__ void __launch_bounds__(NT) rows_streaming_kernel(const RowArgs a)
 template <int NT>
 __global__ void __launch_bounds__(NT) ce_count_kernel(const int64_t *targets, int64_t M, int64_t V,
                                                       int64_t ignore_index, int *n_out,
-                                                      float *loss, int reduction)
+                                                      unsigned *fail, float *loss, int reduction)
 {
     __shared__ int warp_n[NT / 32];
     __shared__ int any_bad;
@@ -1365,6 +1448,7 @@ __global__ void __launch_bounds__(NT) ce_count_kernel(const int64_t *targets, in
             n += __shfl_xor_sync(0xffffffffu, n, off);
         if (threadIdx.x == 0) {
             *n_out = n;
+            *fail = 0u;  // no wait of this call has given up yet
             if (M == 0 && reduction != kReduceNone)  // the mean of nothing is 0/0, the sum 0
                 *loss = reduction == kReduceMean ? __int_as_float(0x7fc00000) : 0.f;
             if (any_bad)
@@ -1375,14 +1459,18 @@ __global__ void __launch_bounds__(NT) ce_count_kernel(const int64_t *targets, in
 
 // L = sum_r row_loss[r] / n after the row kernel (one CTA; launched as its
 // programmatic dependent, it waits for the row kernel to complete first).
+// NaN when a bounded wait of the call gave up (its failure word is set).
 template <int NT>
 __global__ void __launch_bounds__(NT) ce_mean_kernel(const float *row_loss, int64_t M,
-                                                     const int *n_ptr, float *loss, int reduction)
+                                                     const int *n_ptr, const unsigned *fail,
+                                                     float *loss, int reduction)
 {
     wait_prerequisite_grid();
     const float s = sum_row_losses<NT>(row_loss, M, threadIdx.x, 1);
-    if (threadIdx.x == 0)
-        *loss = reduction == kReduceMean ? s / static_cast<float>(__ldcg(n_ptr)) : s;
+    if (threadIdx.x == 0) {
+        const float L = reduction == kReduceMean ? s / static_cast<float>(__ldcg(n_ptr)) : s;
+        *loss = __ldcg(fail) ? __int_as_float(0x7fc00000) : L;
+    }
 }
 
 // x[r, :N] *= scale[per_row ? r : 0], in place (Liger-Kernel cross_entropy.py,

@@ -19,6 +19,15 @@
  * untouched.  Errors that only the device can see (an out-of-range target, a
  * bounded wait that gave up) are raised as sticky per-device flags that
  * gbce_last_error() reports.
+ *
+ * Bounded waits: the staged kernels wait on mbarriers for their own bulk
+ * copies.  Every such wait gives up after 2 s; the CTA then raises
+ * GBCE_ERR_TIMEOUT, stops writing results, waits (again within a fixed
+ * budget) for the copies it has already issued, and exits, so a failed copy
+ * ends the call with an error instead of hanging the device.  Results of a
+ * call that raised GBCE_ERR_TIMEOUT are unspecified inside each operand's rows
+ * [0, cols) (a row the failing CTA had not finished may be partly written);
+ * nothing outside them is written, and the device stays usable.
  */
 #ifndef GBCE_H
 #define GBCE_H
@@ -90,10 +99,14 @@ enum gbce_status {
  *   dtype         GBCE_F32, GBCE_BF16 or GBCE_F16 (logits; targets are always
  *                 int64).  Arithmetic is fp32 with one rounding per stored value.
  *
- * Accuracy: exp(x - m) is evaluated as exp2(fma(x, log2e, -m log2e)); the
- * rounding of m log2e scales with |m|, so the fp32 results stay within 1e-5 of
- * exact while a row's largest logit is within about +-300 (the error grows
- * beyond: about 2e-4 relative at 1e4).
+ * Accuracy: exp(x - m) is evaluated as exp2((x - m) log2e), the difference
+ * formed first, so its error follows the distance |x - m| from the row maximum
+ * and not the logits' magnitude; the row loss is (m - x_t) + ln d.  fp32
+ * results stay within 1e-5 (relative) of exact for any finite logits (tested
+ * with row maxima up to +-1e6 in every kernel regime).
+ *
+ * A bounded wait that gives up (see above) raises GBCE_ERR_TIMEOUT and makes
+ * L NaN; the call's gradient rows are then unspecified as stated above.
  *
  * A target that is neither ignore_index nor in [0, V) leaves its row
  * unmodified, makes L NaN and raises GBCE_ERR_BAD_TARGET in gbce_last_error().
@@ -124,7 +137,9 @@ GBCE_API int ce_fwd_bwd(void *logits, int64_t stride, const int64_t *targets, fl
  *                 when M == 0); not used, and may be NULL, for GBCE_NONE.
  *   row_loss      M floats receiving the row losses l_r (0 for ignored rows, NaN
  *                 for an out-of-range target), 16-byte aligned; required for
- *                 GBCE_NONE, optional (NULL) otherwise.
+ *                 GBCE_NONE, optional (NULL) otherwise.  After GBCE_ERR_TIMEOUT
+ *                 the row losses of rows the failing CTA had not finished are
+ *                 unspecified (a reduced L is NaN).
  *   grad_scale    device floats giving s: NULL means 1; one float for GBCE_MEAN
  *                 and GBCE_SUM; M floats (s_r) for GBCE_NONE.  Read on the device.
  *   reduction     a gbce_reduction, else GBCE_ERR_REDUCTION.
@@ -304,11 +319,42 @@ GBCE_API const char *gbce_plan(int op, int64_t cols, int dtype, int same_phase, 
  * device's sticky error flags.  Returns GBCE_OK, GBCE_ERR_BAD_TARGET,
  * GBCE_ERR_BAD_TABLE or GBCE_ERR_TIMEOUT (the first of these that is set, in
  * this order), or GBCE_ERR_CUDA when the synchronisation itself failed.
+ *
+ * The flags belong to the DEVICE, not to a stream or a call: every call on
+ * the device, from any stream or host thread, raises into the same word, and
+ * the read clears it for all of them.  Only `stream` is synchronised, so a
+ * flag raised by a call still running on another stream may be reported by a
+ * later read instead.  A caller that needs a status per call runs its calls
+ * on one stream, or synchronises every stream that used the device and calls
+ * this once (the result then covers all of those calls).  The cross-entropy
+ * calls also carry their own errors in their result: a bad target or a wait
+ * that gave up makes the reduced loss NaN.
  */
 GBCE_API int gbce_last_error(gbce_stream_t stream);
 
 /* gbce_status_string -- a static, NUL-terminated description of a status code. */
 GBCE_API const char *gbce_status_string(int status);
+
+/*
+ * gbce_pool_reserved -- device memory, in bytes, that the library's scratch
+ * pool holds on `device` (reserved from the driver and kept for reuse), or 0
+ * in *bytes when no call on that device has needed the pool yet.  The pool
+ * serves ce_fwd_bwd, ce_fwd_bwd_ex and ce_fwd_bwd_host; ce_fwd_bwd_noalloc
+ * and the softmax calls never create it.  For diagnostics; no launch, no sync.
+ */
+GBCE_API int gbce_pool_reserved(int device, uint64_t *bytes);
+
+/*
+ * gbce_test_failure_path -- a test of the bounded waits (no counterpart on the
+ * pages).  Makes CTA 0 of every later launch of a staged row kernel
+ * (rows_resident_kernel, rows_ring_kernel) on any device leave out its
+ * `drop_copy`-th bulk copy (counting from 0; -1 leaves none out, the default).
+ * The waits for the missing copy then run out after their 2 s limit and the
+ * GBCE_ERR_TIMEOUT path above runs, with no fault and no hang: such a call
+ * takes a few seconds.  Takes effect for launches made after it returns.  A
+ * process that never calls it never leaves a copy out.
+ */
+GBCE_API int gbce_test_failure_path(int64_t drop_copy);
 
 /*
  * Kernel timing for benchmarks.  While enabled, every ce_fwd_bwd /

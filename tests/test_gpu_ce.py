@@ -224,12 +224,14 @@ def test_other_negative_ignore_index():
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=str)
-@pytest.mark.parametrize("V", [1000, 8000, 100003])   # warp, resident, ring (unaligned rows)
-@pytest.mark.parametrize("offset", [50.0, -150.0, 150.0])
+# warp, resident, ring (unaligned rows), ring split across a cluster
+@pytest.mark.parametrize("V", [1000, 8000, 100003, 262147])
+@pytest.mark.parametrize("offset", [50.0, -150.0, 150.0, 1e4, -1e4, 1e6, -1e6])
 def test_ce_large_logits(dtype, V, offset):
-    """Logits far from zero, up to a row maximum of about 300 in magnitude (the
-    range in which one rounding of m log2e per partial stays within the fp32
-    tolerance): rows with different offsets, one of them ignored."""
+    """Logits far from zero, row maxima up to 2e6 in magnitude, in every kernel
+    regime, within the same tolerances as logits near zero: exp(x - m) is formed
+    from the difference x - m, whose rounding follows |x - m| and not |m|, and
+    the row loss from m - x_y.  Rows with different offsets, one of them ignored."""
     require_gpu()
     M = 6
     g = torch.Generator().manual_seed(V)

@@ -83,14 +83,21 @@ def test_softmax_empty():
     assert gbce.softmax_bwd(x, x).shape == (0, 16)
 
 
-@pytest.mark.parametrize("N", [1000, 4096, 16384, 100003])
-@pytest.mark.parametrize("offset", [50.0, -150.0, 150.0])
+# warp, resident, ring (held rows), ring (streamed, unaligned), ring split across a cluster
+@pytest.mark.parametrize("N", [1000, 4096, 16384, 100003, 300001])
+@pytest.mark.parametrize("offset", [50.0, -150.0, 150.0, 1e4, -1e4, 1e6, -1e6])
 def test_softmax_large_inputs(N, offset):
-    """Inputs far from zero (row maxima up to about 300 in magnitude) keep the
-    forward within the fp32 tolerance."""
+    """Inputs far from zero (row maxima up to 2e6 in magnitude) keep the
+    forward within the fp32 tolerance in every regime, the streaming fallback
+    (x and y at different 16-byte phases) included."""
     require_gpu()
     g = torch.Generator().manual_seed(N)
     x = torch.randn((4, N), generator=g) * 4
     x += torch.tensor([offset, -offset, 0.5 * offset, 2 * offset])[:, None]
     ref = oracle.softmax_fwd(host(x))
     check_softmax(gbce.softmax_fwd(x.cuda()), ref, torch.float32, f"N={N} offset={offset}")
+    xp = torch.zeros((4, N + 1), device="cuda")
+    xp[:, 1:] = x.cuda()
+    check_softmax(gbce.softmax_fwd(xp[:, 1:]), ref, torch.float32,
+                  f"streaming N={N} offset={offset}")
+    assert gbce.last_error() == gbce.OK
