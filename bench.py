@@ -15,6 +15,13 @@ With N > 1 (torchrun) every rank runs its own replica of the workload on its
 own GPU (rows are independent; there is no collective on the data path) and
 the value is the rows of all ranks over the slowest rank's time.
 
+The line also carries ``workloads``: every configuration of the suite (the
+CE workloads 64x1000 fp32, 8192x32000 bf16, 16384x128256 bf16, 4096x250007
+fp32 and its 2-row all-ignored call; the fp32 softmax forward and backward at
+4096 x N, N in {256, 1024, 4096, 16384}), each timed kernel-only with the same
+restore, flush and CUDA-event method, with rows/s, algorithmic GB/s and the
+fraction of the measured copy bandwidth.
+
 ``--impl reference`` times the CPU oracle (double precision, all host cores)
 on a bounded sample of the same workload per step instead.
 """
@@ -38,6 +45,8 @@ import workloads  # noqa: E402
 
 METRIC = "fused CE fwd+bwd rows/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 DEFAULT_WORKLOAD = "ce_bf16_16384x128256"
+# the large-vocabulary CE workloads held to >= 80% of the measured copy bandwidth
+GATED_CE = ("ce_bf16_8192x32000", "ce_bf16_16384x128256", "ce_f32_4096x250007")
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 PROFILE_DIR = os.path.join(ROOT, "profiles")
@@ -378,32 +387,116 @@ def host_link_gbs(x_pinned, reps: int = 3) -> float:
     return x_pinned.numel() * x_pinned.element_size() / (best / 1e3) / 1e9
 
 
-def time_softmax(steps, warmup, ws, flush, N=16384):
-    """Softmax forward, then backward, on the 4096 x N fp32 workload: the
-    kernel time of each call from the library's events, L2 flushed before each."""
+def kernel_ms(call, steps, warmup, flush, ws=1, restore=None):
+    """Mean duration of the library's row kernel in `call` (CUDA events the
+    library records around it on the call's stream), over `steps` calls, each
+    preceded (untimed) by `restore` and an L2 flush; max over ranks.  The calls
+    are enqueued back to back between one barrier + synchronize on each side:
+    a synchronize between a flush and its call would let the start event fire
+    before the host has even enqueued the kernel, timing the launch overhead
+    of short kernels too."""
     import cross_entropy_loss_ce_gb300 as gbce
-    M = workloads.SOFTMAX_M
-    x, y, dy = workloads.make_softmax_inputs(M, N, device="cuda")
-    out = torch.empty_like(x)
-    dx = torch.empty_like(x)
     for _ in range(warmup):
-        gbce.softmax_fwd(x, out)
-        gbce.softmax_bwd(y, dy, dx)
+        if restore:
+            restore()
+        call()
     torch.cuda.synchronize()
-    times = {}
-    for name, call in (("fwd", lambda: gbce.softmax_fwd(x, out)),
-                       ("bwd", lambda: gbce.softmax_bwd(y, dy, dx))):
-        gbce.timing_read()
-        gbce.timing_enable(True)
-        for _ in range(steps):
-            flush_l2(flush)
-            barrier_sync(ws)
-            call()
-        barrier_sync(ws)
-        ms, n = gbce.timing_read()
-        gbce.timing_enable(False)
-        times[name] = max_over_ranks(ms / max(n, 1), ws)
-    return times["fwd"], times["bwd"], M, N
+    if gbce.last_error() != gbce.OK:
+        raise RuntimeError("device error flag raised during warm-up")
+    gbce.timing_read()
+    gbce.timing_enable(True)
+    barrier_sync(ws)
+    for _ in range(steps):
+        if restore:
+            restore()
+        flush_l2(flush)
+        call()
+    barrier_sync(ws)
+    ms, n = gbce.timing_read()
+    gbce.timing_enable(False)
+    if gbce.last_error() != gbce.OK:
+        raise RuntimeError("device error flag raised during the timed calls")
+    return max_over_ranks(ms / max(n, 1), ws)
+
+
+def softmax_traffic(direction: str, M: int, N: int):
+    """DRAM bytes per launch of the softmax row kernel from its committed ncu
+    summary, or None (no summary, or the kernel changed since)."""
+    return profiled_traffic(f"f32_{M}x{N}", f"softmax_{direction}")
+
+
+def entry(workload, kernel, ms, rows, alg_bytes, peak, traffic=None, gated=False, **extra):
+    d = {"workload": workload, "kernel": kernel, "kernel_ms": ms,
+         "rows_per_s": rows / (ms / 1e3), "algorithmic_bytes": alg_bytes,
+         "gbs": alg_bytes / (ms / 1e3) / 1e9, "frac": alg_bytes / (ms / 1e3) / 1e9 / peak,
+         "traffic": traffic, "gated": gated}
+    d.update(extra)
+    return d
+
+
+def ce_workload_entry(w, xd0, td, steps, warmup, flush, peak, ws=1):
+    """One CE workload through ce_fwd_bwd, kernel-only: the row kernel's time,
+    the call's loss checked finite (NaN when every row is ignored)."""
+    import cross_entropy_loss_ce_gb300 as gbce
+    xd = torch.empty_like(xd0)
+    loss = torch.empty((), dtype=torch.float32, device="cuda")
+    ms = kernel_ms(lambda: gbce.ce_fwd_bwd(xd, td, workloads.IGNORE_INDEX, loss), steps, warmup,
+                   flush, ws, restore=lambda: xd.copy_(xd0))
+    t_host = td.cpu().numpy()
+    alg = ce_algorithmic_bytes(w, t_host)
+    kernel, C = gbce.plan("ce", w.V, w.dtype)
+    all_ignored = bool((t_host == workloads.IGNORE_INDEX).all())
+    lv = float(loss.item())
+    if all_ignored != (lv != lv):
+        raise RuntimeError(f"{w.name}: unexpected loss {lv}")
+    gated = w.name in GATED_CE
+    return entry(w.name + (f" (first {w.M} rows, all ignored)" if all_ignored else ""),
+                 f"{kernel}<CE>" + (f", cluster of {C}" if C > 1 else ""), ms, w.M, alg, peak,
+                 None if all_ignored else profiled_traffic(w.name), gated, loss=lv)
+
+
+def softmax_entries(N, steps, warmup, flush, peak, ws=1, M=workloads.SOFTMAX_M):
+    """Softmax forward, then backward, on the M x N fp32 workload (M = 4096)."""
+    import cross_entropy_loss_ce_gb300 as gbce
+    x, y, dy = workloads.make_softmax_inputs(M, N, device="cuda")
+    out = []
+    yo, dx = torch.empty_like(x), torch.empty_like(x)
+    for direction, call, nbytes, op in (
+            ("fwd", lambda: gbce.softmax_fwd(x, yo), 2 * M * N * 4, "softmax_fwd"),
+            ("bwd", lambda: gbce.softmax_bwd(y, dy, dx), 3 * M * N * 4, "softmax_bwd")):
+        ms = kernel_ms(call, steps, warmup, flush, ws)
+        kernel, C = gbce.plan(op, N, torch.float32)
+        out.append(entry(f"softmax_{direction}_f32_{M}x{N}",
+                         f"{kernel}<{op}>" + (f", cluster of {C}" if C > 1 else ""), ms, M,
+                         nbytes, peak, softmax_traffic(direction, M, N), N >= 4096))
+    del x, y, dy, yo, dx
+    return out
+
+
+def all_workloads(steps, warmup, flush, peak, ws=1, c4=None):
+    """Every configuration of the benchmark suite, kernel-only, one entry each:
+    the CE workloads (64x1000 fp32, 8192x32000 bf16, 16384x128256 bf16,
+    4096x250007 fp32 and its 2-row all-ignored call) and the fp32 softmax
+    forward and backward at 4096 x N, N in {256, 1024, 4096, 16384}.  Inputs are
+    drawn on the device.  `c4`: the 16384x128256 inputs when already resident."""
+    out = []
+    for w in workloads.CE_WORKLOADS.values():
+        if c4 is not None and w.name == DEFAULT_WORKLOAD:
+            xd0, td = c4
+        else:
+            xd0, td = workloads.make_ce_inputs(w, "cuda")
+        out.append(ce_workload_entry(w, xd0, td, steps, warmup, flush, peak, ws))
+        if w.name == "ce_f32_4096x250007":
+            w2 = w.with_rows(2)
+            t2 = torch.full((2,), workloads.IGNORE_INDEX, dtype=torch.int64, device="cuda")
+            out.append(ce_workload_entry(w2, xd0[:2].clone(), t2, steps, warmup, flush, peak,
+                                         ws))
+        del xd0, td
+        torch.cuda.empty_cache()
+    for N in workloads.SOFTMAX_NS:
+        out.extend(softmax_entries(N, steps, warmup, flush, peak, ws))
+        torch.cuda.empty_cache()
+    return out
 
 
 def bsr_algorithmic_bytes(meta, Z, es, lut_len) -> int:
@@ -425,21 +518,7 @@ def time_bsr(steps, warmup, ws, flush, peak, heads=0):
         dx = torch.empty_like(dy)
         call = lambda: gbce.softmax_bwd_bsr(y, dy, lut, meta["n_block_rows"], meta["nblocks"],
                                             meta["block"], meta["sizemax"], 1.0, dx)
-        for _ in range(warmup):
-            call()
-        torch.cuda.synchronize()
-        gbce.timing_read()
-        gbce.timing_enable(True)
-        for _ in range(steps):
-            flush_l2(flush)
-            barrier_sync(ws)
-            call()
-        barrier_sync(ws)
-        ms, n = gbce.timing_read()
-        gbce.timing_enable(False)
-        if gbce.last_error() != gbce.OK:
-            raise RuntimeError("device error flag raised")
-        ms = max_over_ranks(ms / max(n, 1), ws)
+        ms = kernel_ms(call, steps, warmup, flush, ws)
         b = bsr_algorithmic_bytes(meta, w.Z, esize(w.dtype), lut.numel())
         rows = w.Z * meta["n_block_rows"] * meta["block"]
         kernel, R = gbce.bsr_plan(meta["block"], meta["sizemax"], w.dtype)
@@ -478,8 +557,7 @@ def run_gbce(args, ws, rank, local):
     achieved = alg / (kavg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": profiled_traffic(w.name),
-                "kernel": ("rows_ring_kernel<CE>" if w.V * esize(w.dtype) > 64 * 1024
-                           else "rows_resident_kernel<CE>"), "kernel_ms": kavg_ms,
+                "kernel": gbce.plan("ce", w.V, w.dtype)[0] + "<CE>", "kernel_ms": kavg_ms,
                 "algorithmic_bytes": alg, "peak_kind": f"{peak_kind} (hbm_gbs, burst)"}
 
     line = {
@@ -500,21 +578,9 @@ def run_gbce(args, ws, rank, local):
         "clocks": clk,
     }
 
-    if not args.no_softmax:
-        fwd_ms, bwd_ms, M, N = time_softmax(max(args.steps // 2, 5), args.warmup, ws, flush)
-        fwd_b, bwd_b = 2 * M * N * 4, 3 * M * N * 4
-        line["softmax"] = {
-            "workload": f"softmax_f32_{M}x{N}", "timing": "row kernel, CUDA events",
-            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-            "fwd_rows_per_s": M / (fwd_ms / 1e3), "bwd_rows_per_s": M / (bwd_ms / 1e3),
-            "fwd_gbs": fwd_b / (fwd_ms / 1e3) / 1e9, "bwd_gbs": bwd_b / (bwd_ms / 1e3) / 1e9,
-            "fwd_frac": fwd_b / (fwd_ms / 1e3) / 1e9 / peak,
-            "bwd_frac": bwd_b / (bwd_ms / 1e3) / 1e9 / peak}
-
-    if not args.no_softmax:
-        line["softmax_bsr"] = time_bsr(max(args.steps // 2, 5), args.warmup, ws, flush, peak)
-
     if not args.no_e2e:
+        # before the per-workload timings: their multi-GB allocations and frees
+        # measurably slow this process's later host-to-device copies
         x_pinned = xd0.cpu().pin_memory()
         t_pinned = td.cpu().pin_memory()
         e2e_ms, h2d, d2h = time_ce_e2e(w, x_pinned, t_pinned, min(args.steps, 10), ws)
@@ -525,6 +591,15 @@ def run_gbce(args, ws, rank, local):
                        "ms_per_step": e2e_ms / e2e_steps,
                        "host_link_h2d_gbs": host_link_gbs(x_pinned)}
         del x_pinned
+
+    if not args.no_workloads:
+        # every configuration, kernel-only, with the same restore, flush and events
+        line["workloads"] = all_workloads(max(args.steps // 5, 10), args.warmup, flush, peak, ws,
+                                          c4=(xd0, td) if w.name == DEFAULT_WORKLOAD and
+                                          not args.rows else None)
+
+    if not args.no_softmax:
+        line["softmax_bsr"] = time_bsr(max(args.steps // 2, 5), args.warmup, ws, flush, peak)
 
     if rank == 0 and not args.no_cpu_baseline:
         sample = min(args.cpu_rows, w.M)
@@ -548,56 +623,42 @@ def run_table(args, local):
     peak, _ = measured_peaks()
     flush = L2Flush()
     steps = max(args.steps // 4, 10)
-
-    def kernel_ms(call, restore=None):
-        for _ in range(args.warmup):
-            if restore:
-                restore()
-            call()
-        torch.cuda.synchronize()
-        gbce.timing_read()
-        gbce.timing_enable(True)
-        for _ in range(steps):
-            if restore:
-                restore()
-            flush_l2(flush)
-            call()
-        torch.cuda.synchronize()
-        ms, n = gbce.timing_read()
-        gbce.timing_enable(False)
-        if gbce.last_error() != gbce.OK:
-            raise RuntimeError("device error flag raised")
-        return ms / max(n, 1)
-
-    for w in workloads.CE_WORKLOADS.values():
-        xd0, td = workloads.make_ce_inputs(w, "cuda")
-        xd = torch.empty_like(xd0)
-        loss = torch.empty((), dtype=torch.float32, device="cuda")
-        ms = kernel_ms(lambda: gbce.ce_fwd_bwd(xd, td, workloads.IGNORE_INDEX, loss),
-                       lambda: xd.copy_(xd0))
-        alg = ce_algorithmic_bytes(w, td.cpu().numpy())
-        print(json.dumps({"table": w.name, "kernel_us": 1e3 * ms, "rows_per_s": w.M / (ms / 1e3),
-                          "alg_gbs": alg / (ms / 1e3) / 1e9,
-                          "frac_of_measured_peak": alg / (ms / 1e3) / 1e9 / peak}), flush=True)
-        del xd0, xd
-        torch.cuda.empty_cache()
-    M = workloads.SOFTMAX_M
-    for N in workloads.SOFTMAX_NS:
-        x, y, dy = workloads.make_softmax_inputs(M, N, device="cuda")
-        out = torch.empty_like(x)
-        for name, call, nb in (("fwd", lambda: gbce.softmax_fwd(x, out), 2),
-                               ("bwd", lambda: gbce.softmax_bwd(y, dy, out), 3)):
-            ms = kernel_ms(call)
-            b = nb * M * N * 4
-            print(json.dumps({"table": f"softmax_{name}_f32_{M}x{N}", "kernel_us": 1e3 * ms,
-                              "rows_per_s": M / (ms / 1e3), "alg_gbs": b / (ms / 1e3) / 1e9,
-                              "frac_of_measured_peak": b / (ms / 1e3) / 1e9 / peak}), flush=True)
-
+    for r in all_workloads(steps, args.warmup, flush, peak):
+        print(json.dumps({"table": r["workload"], "kernel_us": 1e3 * r["kernel_ms"],
+                          "rows_per_s": r["rows_per_s"], "alg_gbs": r["gbs"],
+                          "frac_of_measured_peak": r["frac"], "kernel": r["kernel"]}),
+              flush=True)
     for r in time_bsr(steps, args.warmup, 1, flush, peak):
         print(json.dumps({"table": r["workload"], "kernel_us": 1e3 * r["kernel_ms"],
                           "rows_per_s": r["rows_per_s"], "alg_gbs": r["gbs"],
                           "frac_of_measured_peak": r["frac"], "kernel": r["kernel"],
                           "rows_per_slab_longest": r["rows_per_slab_longest"]}), flush=True)
+
+
+def run_only(args, local):
+    """--only NAME: one workload kernel-only (a CE workload, or softmax_f32_4096xN
+    for the forward and backward), its first --rows rows when given; one JSON
+    line per entry.  A small, single-workload command for profiling."""
+    import cross_entropy_loss_ce_gb300 as gbce
+    gbce.load_library()
+    torch.cuda.set_device(local)
+    peak, _ = measured_peaks()
+    flush = L2Flush()
+    steps = max(args.steps, 1)
+    if args.only in workloads.CE_WORKLOADS:
+        w = workloads.CE_WORKLOADS[args.only]
+        if args.rows:
+            w = w.with_rows(args.rows)
+        xd0, td = workloads.make_ce_inputs(w, "cuda")
+        out = [ce_workload_entry(w, xd0, td, steps, args.warmup, flush, peak)]
+    else:
+        m = re.fullmatch(r"softmax_f32_(\d+)x(\d+)", args.only)
+        if not m:
+            raise SystemExit(f"--only: unknown workload {args.only!r}")
+        out = softmax_entries(int(m.group(2)), steps, args.warmup, flush, peak,
+                              M=args.rows or int(m.group(1)))
+    for r in out:
+        print(json.dumps(r), flush=True)
 
 
 def run_bsr(args, local):
@@ -625,7 +686,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-softmax", action="store_true",
-                    help="skip the row softmax and block-sparse softmax backward timings")
+                    help="skip the block-sparse softmax backward timings")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload kernel timings (every CE and softmax config)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bsr", action="store_true",
                     help="time only the block-sparse softmax backward workloads")
@@ -633,6 +696,9 @@ def main():
                     help="with --bsr: keep this many heads of each workload (profiling)")
     ap.add_argument("--table", action="store_true",
                     help="print the kernel time of every workload instead of the benchmark line")
+    ap.add_argument("--only", default=None,
+                    help="time one workload only: a CE workload name or softmax_f32_4096xN "
+                         "(with --rows: its first ROWS rows); for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -647,6 +713,8 @@ def main():
             run_reference(args, ws, rank)
         elif args.table:
             run_table(args, local)
+        elif args.only:
+            run_only(args, local)
         elif args.bsr:
             run_bsr(args, local)
         else:

@@ -53,3 +53,20 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"] == "ce_bf16_16384x128256"
+
+
+def test_workload_entry_arithmetic():
+    sys.path.insert(0, ROOT)
+    import bench
+    e = bench.entry("w", "k", 2.0, 1000, 4e9, 8000.0, gated=True)
+    assert e["rows_per_s"] == pytest.approx(5e5)
+    assert e["gbs"] == pytest.approx(2000.0) and e["frac"] == pytest.approx(0.25)
+    assert e["gated"] and e["traffic"] is None
+
+
+def test_gated_workloads_are_the_large_vocabulary_ones():
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    assert set(bench.GATED_CE) <= set(workloads.CE_WORKLOADS)
+    assert "ce_f32_64x1000" not in bench.GATED_CE
