@@ -449,7 +449,7 @@ def ce_workload_entry(w, xd0, td, steps, warmup, flush, peak, ws=1):
     lv = float(loss.item())
     if all_ignored != (lv != lv):
         raise RuntimeError(f"{w.name}: unexpected loss {lv}")
-    gated = w.name in GATED_CE
+    gated = w.name in GATED_CE and not all_ignored
     return entry(w.name + (f" (first {w.M} rows, all ignored)" if all_ignored else ""),
                  f"{kernel}<CE>" + (f", cluster of {C}" if C > 1 else ""), ms, w.M, alg, peak,
                  None if all_ignored else profiled_traffic(w.name), gated, loss=lv)
@@ -478,7 +478,9 @@ def all_workloads(steps, warmup, flush, peak, ws=1, c4=None):
     the CE workloads (64x1000 fp32, 8192x32000 bf16, 16384x128256 bf16,
     4096x250007 fp32 and its 2-row all-ignored call) and the fp32 softmax
     forward and backward at 4096 x N, N in {256, 1024, 4096, 16384}.  Inputs are
-    drawn on the device.  `c4`: the 16384x128256 inputs when already resident."""
+    drawn on the device.  `c4`: the 16384x128256 inputs when already resident.
+    A last pair of entries times a one-row softmax (1 KB): the fixed cost of a
+    launch between the two events, which bounds the small shapes."""
     out = []
     for w in workloads.CE_WORKLOADS.values():
         if c4 is not None and w.name == DEFAULT_WORKLOAD:
@@ -496,6 +498,10 @@ def all_workloads(steps, warmup, flush, peak, ws=1, c4=None):
     for N in workloads.SOFTMAX_NS:
         out.extend(softmax_entries(N, steps, warmup, flush, peak, ws))
         torch.cuda.empty_cache()
+    # the fixed cost of one launch between the events: a one-row softmax of 1 KB
+    for e in softmax_entries(256, steps, warmup, flush, peak, ws, M=1):
+        e["workload"] = "launch floor: " + e["workload"]
+        out.append(e)
     return out
 
 
