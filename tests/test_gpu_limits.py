@@ -16,7 +16,7 @@ import cross_entropy_loss_ce_gb300 as gbce
 import oracle
 import workloads
 from gpu_util import require_gpu
-from parity import check_grad, check_grad_factor, check_loss
+from parity import check_grad, check_grad_factor, check_loss, check_softmax
 
 pytestmark = pytest.mark.gpu
 II = workloads.IGNORE_INDEX
@@ -81,3 +81,31 @@ def test_ce_most_columns():
     got = x[0, torch.as_tensor(cols, device="cuda")].reshape(1, -1)
     check_grad_factor(got, ref.reshape(1, -1), np.ones(1), torch.bfloat16,
                       "sampled elements of a 2^31 - 1 column row")
+
+
+def test_softmax_fwd_most_columns():
+    """Softmax forward of one bf16 row of N = 2^31 - 1 (the ring split across a
+    cluster of 16 CTAs): sampled outputs against exp(x_i - lse), where
+    lse = l + x_t is taken from the oracle's cross-entropy loss l of the same
+    row for some column t."""
+    require_gpu()
+    N = MAX_COLS
+    name, C = gbce.plan("softmax_fwd", N, torch.bfloat16)
+    assert name == "rows_ring_kernel" and C == 16
+    g = torch.Generator(device="cuda").manual_seed(13)
+    x = torch.randn((1, N), generator=g, device="cuda", dtype=torch.bfloat16)
+    yv = gbce.softmax_fwd(x)
+    assert gbce.last_error() == gbce.OK
+    xh = x.cpu()
+    del x
+    t = 12345
+    _, row_loss = oracle.ce_rows(oracle.host_array(xh), np.array([t]), N, 1, want_grad=False)
+    lse = float(row_loss[0]) + float(xh[0, t].double())
+    per = -(-(N // 8) // C) * 8
+    rng = np.random.default_rng(7)
+    cols = np.unique(np.concatenate([[0, 1, 7, 8, N - 9, N - 8, N - 2, N - 1],
+                                     [k * per + d for k in range(1, C) for d in (-1, 0)],
+                                     rng.choice(N, 4000, replace=False)]))
+    ref = np.exp(xh[0, torch.as_tensor(cols)].double().numpy() - lse)
+    got = yv[0, torch.as_tensor(cols, device="cuda")].reshape(1, -1)
+    check_softmax(got, ref.reshape(1, -1), torch.bfloat16, "softmax of a 2^31 - 1 column row")
