@@ -91,10 +91,15 @@ def measured_peaks():
 
 
 def kernel_source_hash(paths=KERNEL_SOURCES) -> str:
+    """A digest of the kernel sources with comments and whitespace removed, so
+    that a profile stays valid across edits that change no code."""
     h = hashlib.sha256()
     for p in paths:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,12 +18,14 @@
 //      with no read; a target outside [0, V) raises a flag and leaves the row.
 //   2. pass 1, the online normaliser (same kernel, step 3, "Algorithm 3" of
 //      the online-softmax paper it cites): running maxima m and rescaled sums
-//      d = sum exp(x - m), merged as (m, d) pairs by warp shuffles, through
-//      shared memory, and across a cluster, each sum rescaled to the larger max.
+//      d = sum exp(x - m), kept as (s, d) pairs with s = fl(m log2 e) the shift
+//      in log2 units (see exp2_shift), merged by warp shuffles, through shared
+//      memory, and across a cluster, each sum rescaled to the larger shift.
 //   3. pass 2, the gradient in place (steps 4 and 6): exp(x_i - M) / D times
 //      the row's factor k (1/n for the mean), and (exp(x_y - M) / D - 1) k at
 //      the target, written from the staged copy or registers.
-//   4. the row loss M + ln D - x_y (step 5), x_y read before any store.
+//   4. the row loss M + ln D - x_y (step 5), evaluated as
+//      ln D - (x_y log2 e - S) ln 2, x_y read before any store.
 #pragma once
 
 #include <type_traits>
@@ -726,19 +728,22 @@ __device__ __forceinline__ bool row_is_live(const RowArgs &a, int64_t y)
 }
 
 // ---------------------------------------------------------------------------
-// Warp-specialised ring form (one CTA per row, persistent over rows).
+// Warp-specialised ring form (one CTA, or a cluster of a.C CTAs, per row;
+// persistent over rows).
 //
-// A producer warp streams each live row through a ring of shared-memory
-// chunks with 1-D bulk copies: first the whole row for pass 1, then the row
-// again, chunks in reverse order, for pass 2.  The consumer warps reduce the
-// pass-1 chunks online, merge (m, d) across the CTA, and write the pass-2
-// results.  The ring keeps up to its whole capacity of loads in flight
-// through every phase (including the reduction), and the second read of a
-// row follows the first by one row-time, so it is served by L2: HBM sees one
-// read and one write per element, as with a row held on chip, without
-// splitting rows across SMs.  full[s] (count 1 + bytes) and empty[s] (one
-// arrival per consumer warp) hand each slot back and forth; every wait is
-// bounded.
+// A producer warp streams each live row slice through a ring of shared-memory
+// chunks with 1-D bulk copies: first the whole slice for pass 1, then the
+// slice again, chunks in order, for pass 2 (or once, held for both passes,
+// when it fits half the ring).  The consumer warps reduce the pass-1 chunks
+// online, merge (shift, sum) pairs across the CTA and the cluster, and write
+// the pass-2 results.  The ring keeps up to its whole capacity of loads in
+// flight through every phase (including the reduction), and the second read
+// of a slice follows the first by one slice-time, so it is served by L2: HBM
+// sees one read and one write per element, as with a row held on chip.
+// full[s] (count 1 + bytes) and empty[s] (one arrival per consumer warp) hand
+// each slot back and forth.  Every wait is bounded: a consumer warp that gives
+// up stops releasing slots, a row any warp gave up on gets no stores, and the
+// producer waits for every copy it issued before the CTA exits.
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
