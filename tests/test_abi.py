@@ -41,7 +41,8 @@ def test_header_declares_the_boundary():
     names = set(declared_functions())
     assert {"ce_fwd_bwd", "softmax_fwd", "softmax_bwd", "gbce_last_error",
             "gbce_status_string", "gbce_timing_enable", "gbce_timing_read", "ce_fwd_bwd_ex",
-            "scale_rows", "softmax_bwd_bsr", "gbce_bsr_plan"} <= names
+            "scale_rows", "softmax_bwd_bsr", "gbce_bsr_plan", "ce_fwd_bwd_noalloc",
+            "ce_fwd_bwd_host", "gbce_pool_reserved", "gbce_test_failure_path"} <= names
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -253,3 +254,22 @@ def test_ce_host_rejects_bad_arguments(lib, args, code):
     i64, p, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     lib.ce_fwd_bwd_host.argtypes = [p, i64, p, p, i64, p, i64, i64, i64, ci, p]
     assert lib.ce_fwd_bwd_host(*args, None) == code
+
+
+def test_pool_query_on_the_host(lib):
+    """No call has needed the scratch pool in this process: 0 bytes, no CUDA call."""
+    fn = lib.gbce_pool_reserved
+    fn.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)]
+    v = ctypes.c_uint64(77)
+    assert fn(0, ctypes.byref(v)) == 0 and v.value == 0
+    assert fn(0, None) == 1                      # NULL output
+    assert fn(-1, ctypes.byref(v)) == 2          # no such device slot
+    assert fn(64, ctypes.byref(v)) == 2
+
+
+def test_failure_hook_arguments(lib):
+    fn = lib.gbce_test_failure_path
+    fn.argtypes = [ctypes.c_int64]
+    assert fn(2 ** 40) == 2                      # beyond a 32-bit copy count
+    assert fn(-7) == 0                           # any negative value: no copy left out
+    assert fn(-1) == 0
