@@ -89,6 +89,28 @@ def _call_device(*named):
     return dev
 
 
+class _OnDevice:
+    """Makes `device` current for a library call; a no-op (no context-manager
+    round trip through torch) when it already is, the common case."""
+    __slots__ = ("index", "prev")
+
+    def __init__(self, device):
+        self.index = device.index if device.index is not None else torch.cuda.current_device()
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.index:
+            self.prev = cur
+            torch.cuda.set_device(self.index)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
+
+
 def _stream_handle(stream, device) -> ctypes.c_void_p:
     """The stream of a call on ``device``: the given one (which must belong to
     that device) or the device's current torch stream."""
@@ -135,7 +157,7 @@ def ce_fwd_bwd(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int = 
     elif loss.dtype != torch.float32 or loss.numel() != 1 or not loss.is_cuda:
         raise ValueError("loss must be a one-element float32 CUDA tensor")
     dev = _call_device(("logits", logits), ("targets", targets if M else None), ("loss", loss))
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         rc = load_library().ce_fwd_bwd(lp, stride, targets.data_ptr(), loss.data_ptr(), M, V,
                                        int(ignore_index), DTYPES[logits.dtype],
                                        _stream_handle(stream, dev))
@@ -179,7 +201,7 @@ def ce_fwd_bwd_ex(logits: torch.Tensor, targets: torch.Tensor, ignore_index: int
         gs = _device_floats(grad_scale, M if reduction == "none" else 1, dev, "grad_scale")
     dev = _call_device(("logits", logits), ("targets", targets if M else None), ("loss", loss),
                        ("row_loss", row_loss), ("grad_scale", gs))
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         rc = load_library().ce_fwd_bwd_ex(
             lp, stride, targets.data_ptr(), None if loss is None else loss.data_ptr(),
             None if row_loss is None else row_loss.data_ptr(),
@@ -196,7 +218,7 @@ def scale_rows(x: torch.Tensor, scale, stream=None) -> torch.Tensor:
     per_row = torch.is_tensor(scale) and scale.numel() == M and M != 1
     sc = _device_floats(scale, M if per_row else 1, x.device, "scale")
     dev = _call_device(("x", x), ("scale", sc))
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         rc = load_library().scale_rows(xp, stride, M, N, DTYPES[x.dtype], sc.data_ptr(),
                                        1 if per_row else 0, _stream_handle(stream, dev))
     _check(rc, "scale_rows")
@@ -259,7 +281,7 @@ def softmax_fwd(x: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.T
     if (My, Ny) != (M, N) or y.dtype != x.dtype:
         raise ValueError("y must match x in shape and dtype")
     dev = _call_device(("x", x), ("y", y))
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         rc = load_library().softmax_fwd(xp, xs, yp, ys, M, N, DTYPES[x.dtype],
                                         _stream_handle(stream, dev))
     _check(rc, "softmax_fwd")
@@ -277,7 +299,7 @@ def softmax_bwd(y: torch.Tensor, dy: torch.Tensor, dx: torch.Tensor = None,
     if (Md, Nd) != (M, N) or (Mx, Nx) != (M, N) or not (y.dtype == dy.dtype == dx.dtype):
         raise ValueError("y, dy and dx must share shape and dtype")
     dev = _call_device(("y", y), ("dy", dy), ("dx", dx))
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         rc = load_library().softmax_bwd(yp, ys, dp, ds, xp, xs, M, N, DTYPES[y.dtype],
                                         _stream_handle(stream, dev))
     _check(rc, "softmax_bwd")
@@ -307,7 +329,7 @@ def softmax_bwd_bsr(y: torch.Tensor, dy: torch.Tensor, lut: torch.Tensor, n_bloc
     if lut.dtype != torch.int32 or lut.dim() != 1 or not lut.is_cuda or not lut.is_contiguous():
         raise ValueError("lut must be a contiguous 1-D int32 CUDA tensor")
     dev = _call_device(("y", y), ("dy", dy), ("dx", dx), ("lut", lut))
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         rc = load_library().softmax_bwd_bsr(yp, ys, dp, ds, xp, xs, lut.data_ptr(), lut.numel(),
                                             n_block_rows, nblocks, block, sizemax, Z,
                                             float(scale), DTYPES[y.dtype],
@@ -342,7 +364,7 @@ def last_error(stream=None) -> int:
     """Synchronise the stream and read-and-clear the error flags of its device
     (the current device when no stream is given)."""
     dev = stream.device if stream is not None else torch.device("cuda", torch.cuda.current_device())
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         return load_library().gbce_last_error(_stream_handle(stream, dev))
 
 
@@ -396,7 +418,7 @@ def ce_fwd_bwd_host(logits_host: torch.Tensor, targets_host: torch.Tensor,
                    ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
     fn.restype = ctypes.c_int
     dev = _call_device(("grad", grad))
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         rc = fn(logits_host.data_ptr(), max(hs, V), targets_host.data_ptr(), gp, gs,
                 loss_host.data_ptr(), M, V, int(ignore_index), DTYPES[logits_host.dtype],
                 _stream_handle(stream, dev))
@@ -427,7 +449,7 @@ def ce_fwd_bwd_noalloc(logits: torch.Tensor, targets: torch.Tensor, ignore_index
     fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                    ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
     fn.restype = ctypes.c_int
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         rc = fn(lp, stride, targets.data_ptr(), loss.data_ptr(), M, V, int(ignore_index),
                 DTYPES[logits.dtype], _stream_handle(stream, dev))
     _check(rc, "ce_fwd_bwd_noalloc")
