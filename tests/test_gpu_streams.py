@@ -41,7 +41,7 @@ def test_concurrent_calls_on_two_streams():
         check_loss(float(loss.item()), oracle.ce_mean(ref["row_loss"], ref["n"]), x.dtype)
 
 
-@pytest.mark.parametrize("V", [1000, 32000, 128256])  # warp, resident, ring
+@pytest.mark.parametrize("V", [1000, 32000, 128256, 262147])  # warp, resident, ring, clustered ring
 def test_graph_capture_and_replay(V):
     require_gpu()
     M = 64
