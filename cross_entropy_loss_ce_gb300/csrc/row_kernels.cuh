@@ -606,6 +606,7 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16
         if (ok) {
             // this thread's shift in log2 units (0 if it saw only -inf: its terms are 0)
             const float sL = (m == -INFINITY) ? 0.f : shift_of(m);
+#pragma unroll 2
             for (int j = tid; j < cnt; j += NT) {
                 float f[VEC];
                 E::unpack(ld_shared_v4(buf0 + j * 16u), f);
@@ -642,6 +643,7 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16
     if (ok) {
         if constexpr (OP == Op::SoftmaxBwd) {
             const float sdot = r.x;
+#pragma unroll 2
             for (int j = tid; j < cnt; j += NT) {
                 float fy[VEC], fd[VEC];
                 E::unpack(ld_shared_v4(buf0 + j * 16u), fy);
@@ -665,6 +667,7 @@ __global__ void __launch_bounds__(NT, (OP == Op::SoftmaxFwd && NT == 128) ? 16
                 scale = 1.f / D;
             }
             const int64_t ycol = y - g.head;  // target position relative to the vectors
+#pragma unroll 2
             for (int j = tid; j < cnt; j += NT) {
                 float f[VEC];
                 E::unpack(ld_shared_v4(buf0 + j * 16u), f);
