@@ -1,5 +1,6 @@
-"""Calls on several streams at once, and a CUDA graph capturing ce_fwd_bwd
-(stream-ordered scratch, programmatic dependent launches) replayed on new inputs."""
+"""Calls on several streams at once, and CUDA graphs capturing ce_fwd_bwd
+(stream-ordered scratch, programmatic dependent launches) and the softmax
+calls, replayed on new inputs."""
 import numpy as np
 import pytest
 import torch
@@ -117,3 +118,58 @@ def test_host_calls_on_two_streams():
     assert gbce.last_error() == gbce.OK
     for (ref_g, ref_l), (grad, loss) in zip(refs, outs):
         assert torch.equal(grad, ref_g) and float(loss.item()) == ref_l
+
+
+@pytest.mark.parametrize("N", [1000, 4096, 16384, 300001])  # warp, resident, ring, clustered ring
+def test_softmax_calls_in_a_cuda_graph(N):
+    """softmax_fwd, softmax_bwd and the block-sparse backward captured in one
+    CUDA graph, replayed on new inputs: the results of direct calls, bit for
+    bit, and the oracle's within tolerance."""
+    require_gpu()
+    from parity import check_softmax, check_softmax_bwd
+    M = 6 if N < 100000 else 2
+    w = workloads.BSR_WORKLOADS["bsr_f32_causal_2x16x4096_b32"].with_sizes(Z=1, H=1, S=256)
+    x = torch.empty((M, N), device="cuda")
+    yv, dy = torch.empty_like(x), torch.empty_like(x)
+    y_out, dx_out = torch.empty_like(x), torch.empty_like(x)
+    by, bdy, lut, meta = workloads.make_bsr_inputs(w, device="cuda")
+    bdx = torch.empty_like(bdy)
+    bargs = (meta["n_block_rows"], meta["nblocks"], meta["block"], meta["sizemax"])
+
+    def calls():
+        gbce.softmax_fwd(x, y_out)
+        gbce.softmax_bwd(yv, dy, dx_out)
+        gbce.softmax_bwd_bsr(by, bdy, lut, *bargs, 0.5, bdx)
+
+    def fill(seed):
+        xs, ys, dys = workloads.make_softmax_inputs(M, N, seed=seed)
+        x.copy_(xs.cuda())
+        yv.copy_(ys.cuda())
+        dy.copy_(dys.cuda())
+        by.copy_(torch.rand_like(by))
+        bdy.copy_(torch.randn_like(bdy))
+        return xs, ys, dys
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        fill(0)
+        calls()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls()
+    for seed in (1, 2):
+        xs, ys, dys = fill(seed)
+        graph.replay()
+        torch.cuda.synchronize()
+        got = (y_out.clone(), dx_out.clone(), bdx.clone())
+        calls()
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], y_out) and torch.equal(got[1], dx_out)
+        assert torch.equal(got[2], bdx)
+        check_softmax(got[0], oracle.softmax_fwd(oracle.host_array(xs)), torch.float32,
+                      f"graph softmax N={N}")
+        check_softmax_bwd(got[1], oracle.softmax_bwd(oracle.host_array(ys), oracle.host_array(dys)),
+                          ys, dys, torch.float32, f"graph softmax bwd N={N}")
+    assert gbce.last_error() == gbce.OK
