@@ -449,15 +449,17 @@ def ce_workload_entry(w, xd0, td, steps, warmup, flush, peak, ws=1):
                    flush, ws, restore=lambda: xd.copy_(xd0))
     t_host = td.cpu().numpy()
     alg = ce_algorithmic_bytes(w, t_host)
-    kernel, C = gbce.plan("ce", w.V, w.dtype)
+    kernel, C = gbce.plan("ce", w.M, w.V, w.dtype)
     all_ignored = bool((t_host == workloads.IGNORE_INDEX).all())
     lv = float(loss.item())
     if all_ignored != (lv != lv):
         raise RuntimeError(f"{w.name}: unexpected loss {lv}")
-    gated = w.name in GATED_CE and not all_ignored
-    return entry(w.name + (f" (first {w.M} rows, all ignored)" if all_ignored else ""),
-                 f"{kernel}<CE>" + (f", cluster of {C}" if C > 1 else ""), ms, w.M, alg, peak,
-                 None if all_ignored else profiled_traffic(w.name), gated, loss=lv)
+    full = w.M == workloads.CE_WORKLOADS[w.name].M
+    gated = w.name in GATED_CE and full and not all_ignored
+    name = w.name if full else f"{w.name} (first {w.M} rows" + (", all ignored)" if all_ignored
+                                                                  else ")")
+    return entry(name, f"{kernel}<CE>" + (f", cluster of {C}" if C > 1 else ""), ms, w.M, alg,
+                 peak, profiled_traffic(w.name) if full else None, gated, loss=lv)
 
 
 def softmax_entries(N, steps, warmup, flush, peak, ws=1, M=workloads.SOFTMAX_M):
@@ -470,7 +472,7 @@ def softmax_entries(N, steps, warmup, flush, peak, ws=1, M=workloads.SOFTMAX_M):
             ("fwd", lambda: gbce.softmax_fwd(x, yo), 2 * M * N * 4, "softmax_fwd"),
             ("bwd", lambda: gbce.softmax_bwd(y, dy, dx), 3 * M * N * 4, "softmax_bwd")):
         ms = kernel_ms(call, steps, warmup, flush, ws)
-        kernel, C = gbce.plan(op, N, torch.float32)
+        kernel, C = gbce.plan(op, M, N, torch.float32)
         out.append(entry(f"softmax_{direction}_f32_{M}x{N}",
                          f"{kernel}<{op}>" + (f", cluster of {C}" if C > 1 else ""), ms, M,
                          nbytes, peak, softmax_traffic(direction, M, N), N >= 4096))
@@ -478,12 +480,17 @@ def softmax_entries(N, steps, warmup, flush, peak, ws=1, M=workloads.SOFTMAX_M):
     return out
 
 
+SMALL_BATCH = 8  # rows of the small-batch CE entry
+
+
 def all_workloads(steps, warmup, flush, peak, ws=1, c4=None):
     """Every configuration of the benchmark suite, kernel-only, one entry each:
     the CE workloads (64x1000 fp32, 8192x32000 bf16, 16384x128256 bf16,
     4096x250007 fp32 and its 2-row all-ignored call) and the fp32 softmax
-    forward and backward at 4096 x N, N in {256, 1024, 4096, 16384}.  Inputs are
-    drawn on the device.  `c4`: the 16384x128256 inputs when already resident.
+    forward and backward at 4096 x N, N in {256, 1024, 4096, 16384}; then two
+    small batches: the first 8 rows of the 16384x128256 workload and a one-row
+    fp32 softmax of N = 128256.  Inputs are drawn on the device.  `c4`: the
+    16384x128256 inputs when already resident.
     A last pair of entries times a one-row softmax (1 KB): the fixed cost of a
     launch between the two events, which bounds the small shapes."""
     out = []
@@ -503,6 +510,16 @@ def all_workloads(steps, warmup, flush, peak, ws=1, c4=None):
     for N in workloads.SOFTMAX_NS:
         out.extend(softmax_entries(N, steps, warmup, flush, peak, ws))
         torch.cuda.empty_cache()
+    # small batches of long rows (each row split across a cluster): the first 8
+    # rows of the 128256-column bf16 workload, and one fp32 softmax row of 128256
+    w = workloads.CE_WORKLOADS[DEFAULT_WORKLOAD]
+    if c4 is not None:
+        x8, t8 = c4[0][:SMALL_BATCH].clone(), c4[1][:SMALL_BATCH].clone()
+    else:
+        x8, t8 = workloads.make_ce_inputs(w.with_rows(SMALL_BATCH), "cuda")
+    out.append(ce_workload_entry(w.with_rows(SMALL_BATCH), x8, t8, steps, warmup, flush, peak, ws))
+    del x8, t8
+    out.extend(softmax_entries(128256, steps, warmup, flush, peak, ws, M=1))
     # the fixed cost of one launch between the events: a one-row softmax of 1 KB
     for e in softmax_entries(256, steps, warmup, flush, peak, ws, M=1):
         e["workload"] = "launch floor: " + e["workload"]
@@ -568,7 +585,7 @@ def run_gbce(args, ws, rank, local):
     achieved = alg / (kavg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": profiled_traffic(w.name),
-                "kernel": gbce.plan("ce", w.V, w.dtype)[0] + "<CE>", "kernel_ms": kavg_ms,
+                "kernel": gbce.plan("ce", w.M, w.V, w.dtype)[0] + "<CE>", "kernel_ms": kavg_ms,
                 "algorithmic_bytes": alg, "peak_kind": f"{peak_kind} (hbm_gbs, burst)"}
 
     line = {

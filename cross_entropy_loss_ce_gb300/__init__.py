@@ -44,7 +44,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.softmax_bwd.argtypes = [p, i64, p, i64, p, i64, i64, i64, ci, p]
         lib.ce_fwd_bwd_ex.argtypes = [p, i64, p, p, p, p, i64, i64, i64, ci, ci, p]
         lib.scale_rows.argtypes = [p, i64, i64, i64, ci, p, ci, p]
-        lib.gbce_plan.argtypes = [ci, i64, ci, ci, ctypes.POINTER(ci)]
+        lib.gbce_plan.argtypes = [ci, i64, i64, ci, ci, ctypes.POINTER(ci)]
         lib.gbce_plan.restype = ctypes.c_char_p
         lib.gbce_last_error.argtypes = [p]
         lib.gbce_status_string.argtypes = [ci]
@@ -349,11 +349,12 @@ def bsr_plan(block: int, sizemax: int, dtype: torch.dtype, aligned: bool = True)
     return name.decode(), r.value
 
 
-def plan(op: str, cols: int, dtype: torch.dtype, same_phase: bool = True):
-    """(row-kernel family, CTAs per row) the library picks for rows of `cols`
-    elements on the current device; op is 'ce', 'softmax_fwd' or 'softmax_bwd'."""
+def plan(op: str, M: int, cols: int, dtype: torch.dtype, same_phase: bool = True):
+    """(row-kernel family, CTAs per row) the library picks for M rows of `cols`
+    elements on the current device; op is 'ce', 'softmax_fwd' or 'softmax_bwd'.
+    M matters only for batches of at most one row per SM (gbce_plan)."""
     c = ctypes.c_int(0)
-    name = load_library().gbce_plan({"ce": 0, "softmax_fwd": 1, "softmax_bwd": 2}[op], cols,
+    name = load_library().gbce_plan({"ce": 0, "softmax_fwd": 1, "softmax_bwd": 2}[op], M, cols,
                                     DTYPES[dtype], 1 if same_phase else 0, ctypes.byref(c))
     if name is None:
         raise ValueError("invalid plan query")

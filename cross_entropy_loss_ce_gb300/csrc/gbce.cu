@@ -36,6 +36,13 @@ constexpr int kRingWarpsCluster = 15;         // ... when rows are split across 
 constexpr int kRingVpt1 = 4;                  // vectors per consumer thread and slot, one operand
 constexpr int kRingVpt2 = 2;                  // the same, two operands (softmax backward)
 constexpr int64_t kL2Budget = 40ll << 20;     // bytes of rows between their two reads, all SMs
+constexpr int64_t kSmallBatchStaged = 32 * 1024;  // small batches: rows staging more take the
+                                              // ring (measured: 64 KB rows, 1-152 of them,
+                                              // 5-21% faster there)
+constexpr int64_t kMinClusterRow = 64 * 1024; // ... split across a cluster from this row length
+                                              // on (shorter: the exchange costs more than the
+                                              // split saves, measured on 36-48 KB rows)
+constexpr int64_t kMinSlice = 16 * 1024;      // ... in slices of at least this many bytes
 constexpr int64_t kBsrTarget = 32 * 1024;     // block-sparse: bytes per slab stage aimed at
 constexpr int kBsrThreads = 256;              // block-sparse kernels' CTA size
 constexpr int kBsrMaxRows = 64;               // rows per slab (<= kBsrThreads / 4)
@@ -81,6 +88,29 @@ struct Plan {
     size_t smem;    // dynamic shared memory per CTA
 };
 
+// The ring plan for rows of nvec 16-byte vectors per operand split across a
+// cluster of C CTAs.
+Plan ring_plan(int64_t nvec, int nbuf, int C)
+{
+    Plan p{};
+    p.kind = Kind::Ring;
+    p.C = C;
+    const int ncw = p.C > 1 ? kRingWarpsCluster : kRingWarps;
+    p.nt = (ncw + 1) * 32;
+    const int vpt = nbuf == 2 ? kRingVpt2 : kRingVpt1;
+    const int64_t chunk_bytes = static_cast<int64_t>(ncw) * 32 * vpt * 16;
+    p.chunk_vec = static_cast<int>(chunk_bytes / 16);
+    p.nslot = static_cast<int>(kRingBytes / (chunk_bytes * nbuf));
+    if (p.nslot > kRingMaxSlots)
+        p.nslot = kRingMaxSlots;
+    p.smem = static_cast<size_t>(p.nslot) * chunk_bytes * nbuf;
+    // the most chunks any row slice needs: rows with a head have fewer vectors
+    const int64_t per_max = (nvec + p.C - 1) / p.C;
+    const int64_t nch_max = (per_max + p.chunk_vec - 1) / p.chunk_vec;
+    p.hold = 2 * nch_max <= p.nslot;
+    return p;
+}
+
 // cols elements of esize bytes per operand, nbuf operands per row; `aligned`:
 // all operands of every row share their address modulo 16 bytes.
 Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned,
@@ -123,25 +153,11 @@ Plan make_plan(int64_t cols, size_t esize, int nbuf, bool aligned,
     // long rows: each SM streams one row slice at a time through the ring and
     // reads it twice; split rows across a cluster until the slices between
     // their two reads fit in L2
-    p.kind = Kind::Ring;
     const int64_t sms = current_sm_count();
-    p.C = 1;
-    while (p.C < kMaxCluster && sms * row_bytes * nbuf / p.C > kL2Budget)
-        ++p.C;
-    const int ncw = p.C > 1 ? kRingWarpsCluster : kRingWarps;
-    p.nt = (ncw + 1) * 32;
-    const int vpt = nbuf == 2 ? kRingVpt2 : kRingVpt1;
-    const int64_t chunk_bytes = static_cast<int64_t>(ncw) * 32 * vpt * 16;
-    p.chunk_vec = static_cast<int>(chunk_bytes / 16);
-    p.nslot = static_cast<int>(kRingBytes / (chunk_bytes * nbuf));
-    if (p.nslot > kRingMaxSlots)
-        p.nslot = kRingMaxSlots;
-    p.smem = static_cast<size_t>(p.nslot) * chunk_bytes * nbuf;
-    // the most chunks any row slice needs: rows with a head have fewer vectors
-    const int64_t per_max = (nvec + p.C - 1) / p.C;
-    const int64_t nch_max = (per_max + p.chunk_vec - 1) / p.chunk_vec;
-    p.hold = 2 * nch_max <= p.nslot;
-    return p;
+    int C = 1;
+    while (C < kMaxCluster && sms * row_bytes * nbuf / C > kL2Budget)
+        ++C;
+    return ring_plan(nvec, nbuf, C);
 }
 
 // ---------------------------------------------------------------------------
@@ -365,6 +381,40 @@ cudaError_t resident_clusters(KernelFn fn, const Plan &p, int device, int64_t *o
     return cudaSuccess;
 }
 
+// The plan for a batch of M rows.  make_plan's plan assumes enough rows to
+// fill the device; a batch of at most one row per SM instead goes to the ring
+// (rows that stage more than 32 KB), each row of 64 KB or more per operand
+// split across the largest cluster of which M fit on the device at once, with
+// slices of at least 16 KB: every row is then in flight in one wave, on up to
+// 16 SMs each.  Batches no such cluster takes keep make_plan's plan.
+template <Op OP>
+Plan batch_plan(int dtype, int64_t M, int64_t cols, int nbuf, bool aligned,
+                int64_t resident_max = kResidentMax, int64_t small_cta_vec = 511)
+{
+    const int64_t row_bytes = cols * static_cast<int64_t>(elem_size(dtype));
+    const Plan p = make_plan(cols, elem_size(dtype), nbuf, aligned, resident_max, small_cta_vec);
+    const bool streamed = p.kind == Kind::Ring ||
+                          (p.kind == Kind::Resident && row_bytes * nbuf > kSmallBatchStaged);
+    if (!streamed || M < 1 || M > current_sm_count())
+        return p;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess)
+        return p;
+    const int64_t by_slice = row_bytes < kMinClusterRow ? 1 : row_bytes / kMinSlice;
+    const int cmax = by_slice < 1 ? 1 : (by_slice > kMaxCluster ? kMaxCluster : static_cast<int>(by_slice));
+    const int cmin = p.kind == Kind::Ring ? p.C : 1;
+    for (int C = cmax; C >= cmin; --C) {  // fewer clusters fit as they grow
+        const Plan q = ring_plan(row_bytes / 16, nbuf, C);
+        const KernelFn fn = pick<OP>(dtype, q);
+        int64_t fit = 0;
+        if (configure(fn, device) != cudaSuccess || resident_clusters(fn, q, device, &fit) != cudaSuccess)
+            return p;
+        if (fit >= M)
+            return q;
+    }
+    return p;
+}
+
 // `after_count`: the row kernel follows ce_count_kernel on the stream and may
 // start while it runs (programmatic dependent launch); it waits for it on the
 // device before it reads n.
@@ -477,7 +527,7 @@ cudaError_t launch_ce(void *logits, int64_t stride, const int64_t *targets, floa
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || M == 0)
         return e;
-    const Plan p = make_plan(V, elem_size(dtype), 1, true);
+    const Plan p = batch_plan<Op::CE>(dtype, M, V, 1, true);
     RowArgs a{};
     a.in0 = logits;
     a.s0 = stride;
@@ -698,7 +748,8 @@ cudaError_t launch_ce_host(const void *logits_host, int64_t host_stride,
         cudaEventDestroy(ready);
         if (e != cudaSuccess)
             return e;
-        const Plan p = make_plan(V, es, 1, true);
+        // the device call's plan for all M rows: the same kernel, so the same bits
+        const Plan p = batch_plan<Op::CE>(dtype, M, V, 1, true);
         const KernelFn fn = pick<Op::CE>(dtype, p);
         const int64_t chunks = M < kHostChunks ? M : kHostChunks;
         const int64_t per = (M + chunks - 1) / chunks;
@@ -840,8 +891,9 @@ extern "C" int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_s
     if (M == 0)
         return GBCE_OK;
     const size_t es = elem_size(dtype);
-    const Plan p = make_plan(N, es, 1, same_phase(x, x_stride, y, y_stride, es, M),
-                             kResidentMaxFwd, kSmallCtaVecFwd);
+    const Plan p = batch_plan<Op::SoftmaxFwd>(dtype, M, N, 1,
+                                              same_phase(x, x_stride, y, y_stride, es, M),
+                                              kResidentMaxFwd, kSmallCtaVecFwd);
     RowArgs a{};
     a.in0 = x;
     a.s0 = x_stride;
@@ -873,7 +925,7 @@ extern "C" int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int6
     const size_t es = elem_size(dtype);
     const bool aligned = same_phase(y, y_stride, dy, dy_stride, es, M) &&
                          same_phase(y, y_stride, dx, dx_stride, es, M);
-    const Plan p = make_plan(N, es, 2, aligned);
+    const Plan p = batch_plan<Op::SoftmaxBwd>(dtype, M, N, 2, aligned);
     RowArgs a{};
     a.in0 = y;
     a.s0 = y_stride;
@@ -891,15 +943,17 @@ extern "C" int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int6
                                  reinterpret_cast<cudaStream_t>(stream_)));
 }
 
-extern "C" const char *gbce_plan(int op, int64_t cols, int dtype, int same_phase,
+extern "C" const char *gbce_plan(int op, int64_t M, int64_t cols, int dtype, int same_phase,
                                  int *ctas_per_row)
 {
-    if (op < 0 || op > 2 || cols < 1 ||
+    if (op < 0 || op > 2 || M < 0 || cols < 1 ||
         (dtype != GBCE_F32 && dtype != GBCE_BF16 && dtype != GBCE_F16))
         return nullptr;
-    const Plan p = make_plan(cols, elem_size(dtype), op == 2 ? 2 : 1, same_phase != 0,
-                             op == 1 ? kResidentMaxFwd : kResidentMax,
-                             op == 1 ? kSmallCtaVecFwd : 511);
+    const bool aligned = same_phase != 0;
+    const Plan p = op == 0   ? batch_plan<Op::CE>(dtype, M, cols, 1, aligned)
+                   : op == 1 ? batch_plan<Op::SoftmaxFwd>(dtype, M, cols, 1, aligned,
+                                                          kResidentMaxFwd, kSmallCtaVecFwd)
+                             : batch_plan<Op::SoftmaxBwd>(dtype, M, cols, 2, aligned);
     if (ctas_per_row)
         *ctas_per_row = p.C;
     switch (p.kind) {

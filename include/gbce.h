@@ -302,17 +302,27 @@ GBCE_API const char *gbce_bsr_plan(int64_t block, int64_t sizemax, int dtype, in
                                    int *rows_per_slab);
 
 /*
- * gbce_plan -- the row-kernel family a call uses for rows of `cols` elements
- * of `dtype` on the current device: "rows_warp_kernel" (rows of at most 8 KB
- * per operand, one warp per row), "rows_resident_kernel" (at most 64 KB
- * staged per row, one CTA per row), "rows_ring_kernel" (longer rows streamed
- * through a shared-memory ring, *ctas_per_row CTAs of a cluster per row) or
- * "rows_streaming_kernel" (operands whose rows start at different addresses
- * mod 16 bytes: same_phase == 0).  op: 0 ce_fwd_bwd / ce_fwd_bwd_ex,
- * 1 softmax_fwd, 2 softmax_bwd.  Returns NULL for invalid arguments.  For
- * tests and diagnostics; no kernel is launched.
+ * gbce_plan -- the row-kernel family a call uses for M rows of `cols`
+ * elements of `dtype` on the current device: "rows_warp_kernel" (rows of at
+ * most 8 KB per operand, one warp per row), "rows_resident_kernel" (at most
+ * 64 KB staged per row, one CTA per row), "rows_ring_kernel" (longer rows
+ * streamed through a shared-memory ring, *ctas_per_row CTAs of a cluster per
+ * row) or "rows_streaming_kernel" (operands whose rows start at different
+ * addresses mod 16 bytes: same_phase == 0).  op: 0 ce_fwd_bwd /
+ * ce_fwd_bwd_ex, 1 softmax_fwd, 2 softmax_bwd.
+ *
+ * The plan depends on M only for small batches: when M is at most the
+ * device's SM count and rows stage more than 32 KB, the rows take the ring;
+ * rows of 64 KB or more per operand are split across the largest cluster (at
+ * most 16 CTAs, slices of at least 16 KB) of which M fit on the device at
+ * once, so that the whole batch is in flight in one wave.  When no cluster
+ * size allows that, the plan is the one for large M.  ce_fwd_bwd_host plans
+ * for all of its M rows, like the device call.  Without a usable device the plan for large M is
+ * returned.  Returns NULL for invalid arguments (M < 0 included).  For tests
+ * and diagnostics; no kernel is launched.
  */
-GBCE_API const char *gbce_plan(int op, int64_t cols, int dtype, int same_phase, int *ctas_per_row);
+GBCE_API const char *gbce_plan(int op, int64_t M, int64_t cols, int dtype, int same_phase,
+                               int *ctas_per_row);
 
 /*
  * gbce_last_error -- synchronise `stream`, then read and clear the current

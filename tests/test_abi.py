@@ -149,22 +149,23 @@ def test_empty_calls_are_noops(lib):
 
 
 def test_plan_picks_the_regime_by_row_length(lib):
-    """Host-side plan (no device here, so no cluster split): warp rows up to
-    8 KB per operand, resident up to 64 KB staged (32 KB for the softmax
-    forward), ring beyond, streaming when operands' rows sit at different
-    16-byte phases."""
-    lib.gbce_plan.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
-                              ctypes.POINTER(ctypes.c_int)]
+    """Host-side plan (no device here, so no cluster split and no small-batch
+    plan, whatever M): warp rows up to 8 KB per operand, resident up to 64 KB
+    staged (32 KB for the softmax forward), ring beyond, streaming when
+    operands' rows sit at different 16-byte phases."""
+    lib.gbce_plan.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                              ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     lib.gbce_plan.restype = ctypes.c_char_p
     c = ctypes.c_int()
 
-    def plan(op, cols, dtype, same=1):
-        return lib.gbce_plan(op, cols, dtype, same, ctypes.byref(c)).decode()
+    def plan(op, cols, dtype, same=1, M=4096):
+        return lib.gbce_plan(op, M, cols, dtype, same, ctypes.byref(c)).decode()
 
     assert plan(0, 1000, 0) == "rows_warp_kernel"          # 4000 B fp32
     assert plan(0, 2048, 0) == "rows_warp_kernel"          # exactly 8 KB
     assert plan(0, 2052, 0) == "rows_resident_kernel"
     assert plan(0, 32000, 1) == "rows_resident_kernel"     # 64000 B bf16
+    assert plan(0, 32000, 1, M=1) == "rows_resident_kernel"
     assert plan(0, 32768, 1) == "rows_resident_kernel"     # exactly 64 KB
     assert plan(0, 32776, 1) == "rows_ring_kernel"
     assert plan(2, 8192, 0) == "rows_resident_kernel"      # two 32 KB operands: 64 KB
@@ -174,9 +175,12 @@ def test_plan_picks_the_regime_by_row_length(lib):
     assert plan(1, 16384, 0) == "rows_ring_kernel"         # 64 KB fp32 forward rows
     assert plan(1, 8192, 0, same=0) == "rows_streaming_kernel"
     assert plan(0, 128256, 2) == "rows_ring_kernel"        # fp16
-    assert lib.gbce_plan(3, 10, 0, 1, None) is None
-    assert lib.gbce_plan(0, 0, 0, 1, None) is None
-    assert lib.gbce_plan(0, 10, 7, 1, None) is None
+    assert plan(0, 128256, 2, M=0) == "rows_ring_kernel"
+    assert c.value == 1
+    assert lib.gbce_plan(3, 1, 10, 0, 1, None) is None
+    assert lib.gbce_plan(0, 1, 0, 0, 1, None) is None
+    assert lib.gbce_plan(0, 1, 10, 7, 1, None) is None
+    assert lib.gbce_plan(0, -1, 10, 0, 1, None) is None
 
 
 def test_size_limits(lib):

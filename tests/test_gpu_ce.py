@@ -176,16 +176,17 @@ def test_every_regime_is_exercised():
     """The shapes above reach every row-kernel family on this device,
     including the ring split across a cluster."""
     require_gpu()
-    assert gbce.plan("ce", 1000, torch.float32)[0] == "rows_warp_kernel"
-    assert gbce.plan("ce", 4099, torch.float32)[0] == "rows_resident_kernel"
-    assert gbce.plan("ce", 65537, torch.bfloat16) == ("rows_ring_kernel", 1)
-    name, c = gbce.plan("ce", 262147, torch.float32)
+    M = 4096  # a batch that fills the device
+    assert gbce.plan("ce", M, 1000, torch.float32)[0] == "rows_warp_kernel"
+    assert gbce.plan("ce", M, 4099, torch.float32)[0] == "rows_resident_kernel"
+    assert gbce.plan("ce", M, 65537, torch.bfloat16) == ("rows_ring_kernel", 1)
+    name, c = gbce.plan("ce", M, 262147, torch.float32)
     assert name == "rows_ring_kernel" and c >= 2
-    name, c = gbce.plan("ce", 1000003, torch.float32)
+    name, c = gbce.plan("ce", M, 1000003, torch.float32)
     assert name == "rows_ring_kernel" and c >= 8
-    name, c = gbce.plan("ce", 250007, torch.float32)  # the large-vocabulary fp32 workload
+    name, c = gbce.plan("ce", M, 250007, torch.float32)  # the large-vocabulary fp32 workload
     assert name == "rows_ring_kernel" and c >= 2
-    assert gbce.plan("softmax_fwd", 1000, torch.float32, same_phase=False)[0] == \
+    assert gbce.plan("softmax_fwd", M, 1000, torch.float32, same_phase=False)[0] == \
         "rows_streaming_kernel"
 
 
@@ -224,8 +225,9 @@ def test_other_negative_ignore_index():
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=str)
-# warp, resident, ring (unaligned rows), ring split across a cluster
-@pytest.mark.parametrize("V", [1000, 8000, 100003, 262147])
+# 6 rows: warp, resident, the ring on one CTA (unaligned fp32 rows of 48 KB), the ring on a
+# cluster (unaligned rows; a small batch), the ring on a cluster
+@pytest.mark.parametrize("V", [1000, 8000, 12001, 100003, 262147])
 @pytest.mark.parametrize("offset", [50.0, -150.0, 150.0, 1e4, -1e4, 1e6, -1e6])
 def test_ce_large_logits(dtype, V, offset):
     """Logits far from zero, row maxima up to 2e6 in magnitude, in every kernel

@@ -80,11 +80,15 @@ CE_CASES = [
     # then one of the second read (its row is then partly written)
     ("ce_bf16_16384x128256", 600, 3, True),
     ("ce_bf16_16384x128256", 600, 10, False),
-    # resident kernel: a 64 KB row staged in 8 copies
-    ("ce_bf16_8192x32000", 64, 2, True),
+    # resident kernel: a 64 KB row staged in 8 copies (more rows than SMs:
+    # smaller batches of such rows take the ring)
+    ("ce_bf16_8192x32000", 200, 2, True),
     # ring split across a cluster of 4 CTAs (the rank-0 CTA of cluster 0 fails;
     # its peers see the failure in the exchange and write nothing either)
     ("ce_f32_4096x250007", 40, 1, True),
+    # a small batch: 4 rows in one wave, each split across a cluster of 8 or
+    # more CTAs; CTA 0 holds the first slice of row 0 in a single copy
+    ("ce_bf16_16384x128256", 4, 0, True),
 ]
 
 
@@ -125,8 +129,9 @@ def test_ce_wait_that_runs_out(failure_path, name, rows, drop, first_read):
     assert outside_untouched(buf, view)
 
 
-# (N, rows, copy left out): ring with held 64 KB rows, resident 16 KB rows
-SOFTMAX_FWD_CASES = [(16384, 400, 0), (16384, 400, 5), (4096, 64, 1)]
+# (N, rows, copy left out): ring with held 64 KB rows, resident 16 KB rows,
+# and a small batch of 500 KB rows, each split across a cluster
+SOFTMAX_FWD_CASES = [(16384, 400, 0), (16384, 400, 5), (4096, 64, 1), (128256, 3, 0)]
 
 
 @pytest.mark.parametrize("N,rows,drop", SOFTMAX_FWD_CASES)

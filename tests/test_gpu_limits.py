@@ -57,7 +57,7 @@ def test_ce_most_columns():
     boundaries) against exp(x_i - x_y - l) from the oracle's loss."""
     require_gpu()
     V = MAX_COLS
-    name, C = gbce.plan("ce", V, torch.bfloat16)
+    name, C = gbce.plan("ce", 1, V, torch.bfloat16)
     assert name == "rows_ring_kernel" and C == 16
     g = torch.Generator(device="cuda").manual_seed(12)
     x = torch.randn((1, V), generator=g, device="cuda", dtype=torch.bfloat16)
@@ -90,7 +90,7 @@ def test_softmax_fwd_most_columns():
     row for some column t."""
     require_gpu()
     N = MAX_COLS
-    name, C = gbce.plan("softmax_fwd", N, torch.bfloat16)
+    name, C = gbce.plan("softmax_fwd", 1, N, torch.bfloat16)
     assert name == "rows_ring_kernel" and C == 16
     g = torch.Generator(device="cuda").manual_seed(13)
     x = torch.randn((1, N), generator=g, device="cuda", dtype=torch.bfloat16)

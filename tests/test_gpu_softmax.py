@@ -83,8 +83,9 @@ def test_softmax_empty():
     assert gbce.softmax_bwd(x, x).shape == (0, 16)
 
 
-# warp, resident, ring (held rows), ring (streamed, unaligned), ring split across a cluster
-@pytest.mark.parametrize("N", [1000, 4096, 16384, 100003, 300001])
+# 4 rows: warp, resident, the ring on one CTA (48 KB unaligned rows), the ring on a cluster
+# (a small batch: 64 KB rows, unaligned 400 KB rows), the ring on a cluster (the L2 bound)
+@pytest.mark.parametrize("N", [1000, 4096, 12001, 16384, 100003, 300001])
 @pytest.mark.parametrize("offset", [50.0, -150.0, 150.0, 1e4, -1e4, 1e6, -1e6])
 def test_softmax_large_inputs(N, offset):
     """Inputs far from zero (row maxima up to 2e6 in magnitude) keep the

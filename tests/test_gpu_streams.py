@@ -42,7 +42,9 @@ def test_concurrent_calls_on_two_streams():
         check_loss(float(loss.item()), oracle.ce_mean(ref["row_loss"], ref["n"]), x.dtype)
 
 
-@pytest.mark.parametrize("V", [1000, 32000, 128256, 262147])  # warp, resident, ring, clustered ring
+# 64 rows each: warp, resident, the ring on one CTA (40 KB rows), the ring on a cluster of 2
+# (a batch under one row per SM), the ring on a cluster of 2 (the L2 bound)
+@pytest.mark.parametrize("V", [1000, 16000, 20001, 128256, 262147])
 def test_graph_capture_and_replay(V):
     require_gpu()
     M = 64
@@ -120,7 +122,9 @@ def test_host_calls_on_two_streams():
         assert torch.equal(grad, ref_g) and float(loss.item()) == ref_l
 
 
-@pytest.mark.parametrize("N", [1000, 4096, 16384, 300001])  # warp, resident, ring, clustered ring
+# warp, resident, ring on one CTA (48 KB rows), ring on a cluster (small batches of 64 KB
+# rows and longer)
+@pytest.mark.parametrize("N", [1000, 4096, 12001, 16384, 300001])
 def test_softmax_calls_in_a_cuda_graph(N):
     """softmax_fwd, softmax_bwd and the block-sparse backward captured in one
     CUDA graph, replayed on new inputs: the results of direct calls, bit for
