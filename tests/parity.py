@@ -58,20 +58,25 @@ def _report(bad, got, ref, tol, what):
         raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance; {details}")
 
 
-def check_grad(got: torch.Tensor, ref: np.ndarray, n: int, dtype, what="gradient"):
+def check_grad(got: torch.Tensor, ref: np.ndarray, n: int, dtype, what="gradient",
+               targets=None):
     g = to_f64(got)
     ref = np.asarray(ref, dtype=np.float64)
     assert g.shape == ref.shape
     check_grad_factor(got, ref, np.full(g.shape[0], 1.0 / n) if n else np.ones(g.shape[0]),
-                      dtype, what)
+                      dtype, what, targets=targets)
 
 
-def check_grad_factor(got, ref, k_rows, dtype, what="gradient", rescaled_by=None):
+def check_grad_factor(got, ref, k_rows, dtype, what="gradient", rescaled_by=None, targets=None):
     """Gradient rows (p - onehot) * k_r: for 16-bit storage the stated 2e-2 bound
     applies to (p - onehot), i.e. |g - o| <= 2e-2 |k_r|; and the relative bound
     of one rounding.  `rescaled_by` (per row) marks a gradient stored once and
     then multiplied by that factor and stored again (the autograd backward): two
-    roundings, the first one's absolute floor amplified by the factor."""
+    roundings, the first one's absolute floor amplified by the factor.
+    `targets` (per row, optional) marks the on-target elements for the fp32
+    bound on (p_y - 1) k; without it an element is on target when its value's
+    sign differs from k's, which misses an exact 0 (p_y = 1: a row of one
+    column, or every other logit more than ~745 below the target's)."""
     g = to_f64(got)
     ref = np.asarray(ref, dtype=np.float64)
     assert g.shape == ref.shape
@@ -87,8 +92,12 @@ def check_grad_factor(got, ref, k_rows, dtype, what="gradient", rescaled_by=None
                 what + " (2e-2 on p - onehot)")
     tol = rel * np.abs(ref) + amp * floor
     if dtype == torch.float32:
-        # the on-target element (p_y - 1) k is the one whose sign differs from k's
-        tol = np.where(ref * k < 0, np.maximum(tol, rel * np.abs(k) + amp * floor), tol)
+        if targets is not None:
+            t = np.asarray(targets, dtype=np.int64)[:, None]
+            on_target = np.arange(g.shape[1])[None, :] == t
+        else:  # the on-target element (p_y - 1) k is the one whose sign differs from k's
+            on_target = ref * k < 0
+        tol = np.where(on_target, np.maximum(tol, rel * np.abs(k) + amp * floor), tol)
     _report(~(np.abs(g - ref) <= tol), g, ref, tol, what)
 
 
