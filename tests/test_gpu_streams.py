@@ -177,3 +177,98 @@ def test_softmax_calls_in_a_cuda_graph(N):
         check_softmax_bwd(got[1], oracle.softmax_bwd(oracle.host_array(ys), oracle.host_array(dys)),
                           ys, dys, torch.float32, f"graph softmax bwd N={N}")
     assert gbce.last_error() == gbce.OK
+
+
+_THREADS_CHILD = r'''
+import sys, threading
+import torch
+import cross_entropy_loss_ce_gb300 as gbce
+
+gbce.load_library()
+torch.zeros(1, device="cuda")
+II = -100
+# per thread: shapes whose first use makes the library plan (small-batch cluster
+# searches included), configure kernels and query occupancy
+SHAPES = [[("ce", 1, 128256, torch.bfloat16), ("fwd", 3, 100003, torch.float32), ("bwd", 40, 6000, torch.float32)],
+          [("ce", 8, 128256, torch.bfloat16), ("ce", 200, 32000, torch.bfloat16), ("fwd", 6, 16384, torch.float32)],
+          [("ce", 33, 250007, torch.float32), ("bwd", 2, 300001, torch.bfloat16), ("ce", 64, 1000, torch.float32)],
+          [("ce", 5, 130001, torch.float16), ("fwd", 152, 32000, torch.float32), ("bwd", 9, 128256, torch.float32)],
+          [("ce", 16, 65537, torch.bfloat16), ("fwd", 1, 2000003, torch.bfloat16), ("ce", 7, 20001, torch.bfloat16)],
+          [("bwd", 24, 20000, torch.float32), ("ce", 100, 128256, torch.bfloat16), ("fwd", 400, 3000, torch.float16)]]
+ROUNDS = 6
+
+def inputs(op, M, N, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    a = (torch.randn((M, N), generator=g) * 3).to(dtype).cuda()
+    b = torch.randn((M, N), generator=g).to(dtype).cuda()
+    t = torch.randint(0, N, (M,), generator=g).cuda()
+    return a, b, t
+
+def run(op, a, b, t):
+    if op == "ce":
+        x = a.clone()
+        loss = gbce.ce_fwd_bwd(x, t, II)
+        return x, loss
+    if op == "fwd":
+        return gbce.softmax_fwd(a), None
+    return gbce.softmax_bwd(torch.softmax(a.float(), 1).to(a.dtype), b), None
+
+results, errors = {}, []
+data = {(i, j): inputs(*SHAPES[i][j], seed=100 * i + j) for i in range(len(SHAPES)) for j in range(3)}
+torch.cuda.synchronize()
+barrier = threading.Barrier(len(SHAPES))
+
+def worker(i):
+    try:
+        s = torch.cuda.Stream()
+        barrier.wait()
+        with torch.cuda.stream(s):
+            for r in range(ROUNDS):
+                for j, (op, M, N, dtype) in enumerate(SHAPES[i]):
+                    a, b, t = data[(i, j)]
+                    results[(i, j, r)] = run(op, a, b, t)
+        s.synchronize()
+    except Exception as e:  # reported by the parent
+        errors.append(f"thread {i}: {e!r}")
+
+threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(SHAPES))]
+for th in threads: th.start()
+for th in threads: th.join()
+torch.cuda.synchronize()
+status = gbce.last_error()
+if errors or status != gbce.OK:
+    print("FAIL", errors, status); sys.exit(1)
+# the same calls once more, one after another: every threaded result is bit-identical
+bad = []
+for i in range(len(SHAPES)):
+    for j, (op, M, N, dtype) in enumerate(SHAPES[i]):
+        ref, lref = run(op, *data[(i, j)])
+        torch.cuda.synchronize()
+        for r in range(ROUNDS):
+            got, lgot = results[(i, j, r)]
+            same = torch.equal(got.view(torch.int16) if got.dtype != torch.float32 else got.view(torch.int32),
+                               ref.view(torch.int16) if ref.dtype != torch.float32 else ref.view(torch.int32))
+            if lref is not None:
+                same = same and torch.equal(lgot.view(torch.int32), lref.view(torch.int32))
+            if not same:
+                bad.append((i, j, r, op, M, N))
+print("FAIL", bad) if bad else print("ok", len(results))
+sys.exit(1 if bad else 0)
+'''
+
+
+def test_first_use_from_several_host_threads():
+    """Six host threads, each on its own stream, start at once in a fresh
+    process and call the library on shapes whose first use plans (small-batch
+    cluster searches included), configures kernels, queries occupancy and
+    creates the scratch pool: every result is bit-identical to the same call
+    made afterwards from one thread, and no error flag is raised."""
+    require_gpu()
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    r = subprocess.run([sys.executable, "-c", _THREADS_CHILD], cwd=root, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
