@@ -248,3 +248,51 @@ def test_ce_large_logits(dtype, V, offset):
     assert status == gbce.OK
     check_grad(xd, ref["grad"], ref["n"], dtype, f"V={V} offset={offset}")
     check_loss(loss, oracle.ce_mean(ref["row_loss"], ref["n"]), dtype, f"V={V} offset={offset}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16], ids=str)
+@pytest.mark.parametrize("V", [1000, 8000, 32000, 128256, 250007])
+@pytest.mark.parametrize("M", [6, 200])
+def test_ce_masked_logits(dtype, V, M):
+    """-inf logits (never at the target) take no probability in every regime:
+    rows with a short finite prefix, a -inf first half, a random -inf half,
+    one finite entry (p_y = 1: loss 0, gradient 0 up to one rounding), and
+    only the last entry finite; the gradient is exactly 0 at every -inf."""
+    require_gpu()
+    if M * V > 30_000_000:
+        pytest.skip("large batch of long rows: covered by the 6-row case")
+    g = torch.Generator().manual_seed(V + M)
+    x = torch.randn((M, V), generator=g) * 3
+    t = torch.empty((M,), dtype=torch.int64)
+    ninf = float("-inf")
+    for r in range(M):
+        kind = r % 6
+        if kind == 0:
+            x[r, min(5, V):] = ninf
+            t[r] = int(torch.randint(0, min(5, V), (1,), generator=g))
+        elif kind == 1:
+            x[r, : V // 2] = ninf
+            t[r] = V // 2 + int(torch.randint(0, V - V // 2, (1,), generator=g))
+        elif kind == 2:
+            x[r, torch.rand(V, generator=g) < 0.5] = ninf
+            t[r] = int(torch.randint(0, V, (1,), generator=g))
+            x[r, t[r]] = 0.5
+        elif kind == 3:
+            t[r] = int(torch.randint(0, V, (1,), generator=g))
+            v = float(x[r, t[r]])
+            x[r] = ninf
+            x[r, t[r]] = v
+        elif kind == 4:
+            t[r] = II if r == 4 else int(torch.randint(0, V, (1,), generator=g))
+        else:
+            x[r, : V - 1] = ninf
+            t[r] = V - 1
+    x = x.to(dtype)
+    ref = oracle_ce(x, t)
+    xd = x.cuda()
+    loss, status = run_ce(xd, t.cuda())
+    assert status == gbce.OK
+    what = f"masked CE {M}x{V} {dtype}, plan {gbce.plan('ce', M, V, dtype)}"
+    check_grad(xd, ref["grad"], ref["n"], dtype, what, targets=t.numpy())
+    check_loss(loss, oracle.ce_mean(ref["row_loss"], ref["n"]), dtype, what)
+    assert bool(torch.all(xd.cpu()[torch.isinf(x)] == 0)), "a -inf logit got a gradient"

@@ -102,3 +102,56 @@ def test_softmax_large_inputs(N, offset):
     check_softmax(gbce.softmax_fwd(xp[:, 1:]), ref, torch.float32,
                   f"streaming N={N} offset={offset}")
     assert gbce.last_error() == gbce.OK
+
+
+def _masked_rows(M, N, dtype, seed):
+    """Rows with -inf entries as an attention mask leaves them: a short finite
+    prefix (the rest -inf: whole chunks and cluster slices of -inf at the
+    end), a -inf first half (the online maximum starts from -inf), a random
+    half, one finite entry, an unmasked row, and only the last entry finite;
+    then the same patterns again."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((M, N), generator=g) * 3
+    ninf = float("-inf")
+    for r in range(M):
+        kind = r % 6
+        if kind == 0:
+            x[r, min(5, N):] = ninf
+        elif kind == 1:
+            x[r, : N // 2] = ninf
+        elif kind == 2:
+            x[r, torch.rand(N, generator=g) < 0.5] = ninf
+            x[r, int(torch.randint(0, N, (1,), generator=g))] = 1.0
+        elif kind == 3:
+            keep = int(torch.randint(0, N, (1,), generator=g))
+            v = float(x[r, keep])
+            x[r] = ninf
+            x[r, keep] = v
+        elif kind == 5:
+            x[r, : N - 1] = ninf
+    return x.to(dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16], ids=str)
+@pytest.mark.parametrize("N", [1000, 4096, 12001, 100003, 300001])
+@pytest.mark.parametrize("M", [6, 200])
+def test_softmax_masked_rows(dtype, N, M):
+    """-inf entries take exactly zero probability in every regime (warp,
+    resident, the ring on one CTA, clusters for small batches and for the L2
+    bound), forward and backward against the oracle."""
+    require_gpu()
+    if M * N > 30_000_000:
+        pytest.skip("large batch of long rows: covered by the 6-row case")
+    x = _masked_rows(M, N, dtype, seed=N + M)
+    ref = oracle.softmax_fwd(host(x))
+    y = gbce.softmax_fwd(x.cuda())
+    assert gbce.last_error() == gbce.OK
+    check_softmax(y, ref, dtype, f"masked softmax {M}x{N}")
+    assert bool(torch.all(y.cpu()[torch.isinf(x)] == 0)), "a -inf entry got probability"
+    yh = y.cpu()
+    g = torch.Generator().manual_seed(N)
+    dy = torch.randn((M, N), generator=g).to(dtype)
+    ref_dx = oracle.softmax_bwd(host(yh), host(dy))
+    dx = gbce.softmax_bwd(y, dy.cuda())
+    assert gbce.last_error() == gbce.OK
+    check_softmax_bwd(dx, ref_dx, yh, dy, dtype, f"masked softmax backward {M}x{N}")
