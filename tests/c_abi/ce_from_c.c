@@ -1,17 +1,24 @@
 /*
  * The library called from plain C, with nothing but the CUDA runtime: the
- * fused cross-entropy and the softmax forward on inputs read from a file.
+ * fused cross-entropy (mean, and with reduction none, per-row losses and a
+ * per-row gradient scale), the softmax forward and backward, and the plan
+ * query, on inputs read from a file.
  *
  *   ce_from_c <in.bin> <out.bin>
  *
- * in.bin:  int64 M, int64 V, then M*V fp32 logits (row-major), M int64 targets.
- * out.bin: float loss, int32 status of the calls, int32 gbce_last_error, then
- *          M*V fp32 gradients (d loss / d logits) and M*V fp32 softmax outputs.
+ * in.bin:  int64 M, int64 V, then M*V fp32 logits (row-major), M int64 targets,
+ *          M*V fp32 upstream gradients dy, M fp32 gradient scales s_r.
+ * out.bin: float loss, int32 status of the calls, int32 gbce_last_error,
+ *          M*V fp32 gradients of the mean loss, M*V fp32 softmax outputs y,
+ *          M*V fp32 softmax backward outputs dx (of y and dy),
+ *          M*V fp32 gradients with reduction none scaled by s_r, M fp32 row
+ *          losses, int32 CTAs per row of the plan, 32 bytes of its kernel name.
  * Exit status 0 when every call returned GBCE_OK and the files were handled.
  */
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <cuda_runtime.h>
 
@@ -21,6 +28,18 @@ static int fail(const char *what)
 {
     fprintf(stderr, "ce_from_c: %s\n", what);
     return 1;
+}
+
+static int to_device(void **dst, const void *src, size_t bytes)
+{
+    if (cudaMalloc(dst, bytes) != cudaSuccess)
+        return 1;
+    return src && cudaMemcpy(*dst, src, bytes, cudaMemcpyHostToDevice) != cudaSuccess;
+}
+
+static int to_host(void *dst, const void *src, size_t bytes)
+{
+    return cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost) != cudaSuccess;
 }
 
 int main(int argc, char **argv)
@@ -33,64 +52,73 @@ int main(int argc, char **argv)
     int64_t M = 0, V = 0;
     if (fread(&M, 8, 1, in) != 1 || fread(&V, 8, 1, in) != 1 || M < 1 || V < 1)
         return fail("bad header");
-    const size_t n = (size_t)M * (size_t)V;
-    float *logits = malloc(n * sizeof(float));
-    float *grad = malloc(n * sizeof(float));
-    float *soft = malloc(n * sizeof(float));
-    int64_t *targets = malloc((size_t)M * sizeof(int64_t));
-    if (!logits || !grad || !soft || !targets)
+    const size_t n = (size_t)M * (size_t)V, mb = (size_t)M;
+    float *logits = malloc(n * 4), *dy = malloc(n * 4), *scale = malloc(mb * 4);
+    float *out = malloc(n * 4), *row_loss = malloc(mb * 4);
+    int64_t *targets = malloc(mb * 8);
+    if (!logits || !dy || !scale || !out || !row_loss || !targets)
         return fail("out of host memory");
-    if (fread(logits, sizeof(float), n, in) != n ||
-        fread(targets, sizeof(int64_t), (size_t)M, in) != (size_t)M)
+    if (fread(logits, 4, n, in) != n || fread(targets, 8, mb, in) != mb ||
+        fread(dy, 4, n, in) != n || fread(scale, 4, mb, in) != mb)
         return fail("short input");
     fclose(in);
 
-    float *d_logits = NULL, *d_soft = NULL, *d_loss = NULL;
-    int64_t *d_targets = NULL;
+    void *d_logits, *d_logits2, *d_soft, *d_dy, *d_scale, *d_loss, *d_row_loss, *d_targets;
     cudaStream_t stream;
-    if (cudaStreamCreate(&stream) != cudaSuccess ||
-        cudaMalloc((void **)&d_logits, n * sizeof(float)) != cudaSuccess ||
-        cudaMalloc((void **)&d_soft, n * sizeof(float)) != cudaSuccess ||
-        cudaMalloc((void **)&d_loss, sizeof(float)) != cudaSuccess ||
-        cudaMalloc((void **)&d_targets, (size_t)M * sizeof(int64_t)) != cudaSuccess)
-        return fail("device allocation failed");
-    if (cudaMemcpy(d_logits, logits, n * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemcpy(d_targets, targets, (size_t)M * sizeof(int64_t), cudaMemcpyHostToDevice) !=
-            cudaSuccess)
-        return fail("copy to the device failed");
+    if (cudaStreamCreate(&stream) != cudaSuccess || to_device(&d_logits, logits, n * 4) ||
+        to_device(&d_logits2, logits, n * 4) || to_device(&d_soft, NULL, n * 4) ||
+        to_device(&d_dy, dy, n * 4) || to_device(&d_scale, scale, mb * 4) ||
+        to_device(&d_loss, NULL, 4) || to_device(&d_row_loss, NULL, mb * 4) ||
+        to_device(&d_targets, targets, mb * 8))
+        return fail("device allocation or copy failed");
 
     gbce_stream_t s = (gbce_stream_t)stream;
-    /* the softmax of the logits first (out of place), then the fused CE in place */
+    /* the softmax of the logits (out of place), its backward in place over dy,
+       the fused CE in place (mean), then with reduction none on a second copy */
     int rc = softmax_fwd(d_logits, V, d_soft, V, M, V, GBCE_F32, s);
     if (rc == GBCE_OK)
+        rc = softmax_bwd(d_soft, V, d_dy, V, d_dy, V, M, V, GBCE_F32, s);
+    if (rc == GBCE_OK)
         rc = ce_fwd_bwd(d_logits, V, d_targets, d_loss, M, V, -100, GBCE_F32, s);
+    if (rc == GBCE_OK)
+        rc = ce_fwd_bwd_ex(d_logits2, V, d_targets, NULL, d_row_loss, d_scale, M, V, -100,
+                           GBCE_F32, GBCE_NONE, s);
     const int flags = gbce_last_error(s);
     if (rc != GBCE_OK)
         fprintf(stderr, "ce_from_c: %s\n", gbce_status_string(rc));
+    int ctas = 0;
+    char name[32] = {0};
+    const char *plan = gbce_plan(0, M, V, GBCE_F32, 1, &ctas);
+    if (!plan)
+        return fail("the plan query failed");
+    strncpy(name, plan, sizeof name - 1);
 
     float loss = 0.f;
-    if (cudaMemcpy(&loss, d_loss, sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemcpy(grad, d_logits, n * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemcpy(soft, d_soft, n * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)
-        return fail("copy from the device failed");
-
-    FILE *out = fopen(argv[2], "wb");
-    if (!out)
+    FILE *o = fopen(argv[2], "wb");
+    if (!o)
         return fail("cannot open the output");
     const int32_t status[2] = {rc, flags};
-    if (fwrite(&loss, sizeof(float), 1, out) != 1 || fwrite(status, 4, 2, out) != 2 ||
-        fwrite(grad, sizeof(float), n, out) != n || fwrite(soft, sizeof(float), n, out) != n)
-        return fail("short output");
-    fclose(out);
+    int bad = to_host(&loss, d_loss, 4) || fwrite(&loss, 4, 1, o) != 1 ||
+              fwrite(status, 4, 2, o) != 2;
+    const void *blocks[4] = {d_logits, d_soft, d_dy, d_logits2};
+    for (int b = 0; b < 4 && !bad; ++b)
+        bad = to_host(out, blocks[b], n * 4) || fwrite(out, 4, n, o) != n;
+    if (!bad)
+        bad = to_host(row_loss, d_row_loss, mb * 4) || fwrite(row_loss, 4, mb, o) != mb ||
+              fwrite(&ctas, 4, 1, o) != 1 || fwrite(name, 1, sizeof name, o) != sizeof name;
+    fclose(o);
+    if (bad)
+        return fail("copy from the device or output failed");
 
-    cudaFree(d_logits);
-    cudaFree(d_soft);
-    cudaFree(d_loss);
-    cudaFree(d_targets);
+    void *bufs[8] = {d_logits, d_logits2, d_soft, d_dy, d_scale, d_loss, d_row_loss, d_targets};
+    for (int b = 0; b < 8; ++b)
+        cudaFree(bufs[b]);
     cudaStreamDestroy(stream);
     free(logits);
-    free(grad);
-    free(soft);
+    free(dy);
+    free(scale);
+    free(out);
+    free(row_loss);
     free(targets);
     return (rc == GBCE_OK && flags == GBCE_OK) ? 0 : 2;
 }
