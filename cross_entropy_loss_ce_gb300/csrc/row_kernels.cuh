@@ -1195,7 +1195,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                 auto chunk2 = [&](auto full_tag) {
                     constexpr bool FULL = decltype(full_tag)::value;
                     const uint32_t b0 = ring + slot * kSlotBytes;
-                    uint4 raw[VPT], raw2[VPT];
+                    uint4 raw[VPT];
+                    [[maybe_unused]] uint4 raw2[VPT];  // the second operand (softmax backward)
 #pragma unroll
                     for (int v = 0; v < VPT; ++v) {
                         const int j = tid + v * NC;
