@@ -52,6 +52,23 @@ constexpr int kBsrLog2MinSlabs = 3;           // ... each keeping >= 8 slabs of 
 
 size_t elem_size(int dtype) { return dtype == GBCE_F32 ? 4 : 2; }
 
+// The library's one-time set-up (the scratch pool, kernel attributes,
+// occupancy queries, the static scratch array's address) may run while the
+// calling thread captures a CUDA graph: a first call can be a captured one.
+// The default (global) capture mode refuses such calls; none of them touches
+// a stream, so they run with the thread switched to relaxed mode, which
+// allows them, and the thread's mode is restored after.
+class RelaxedCapture {
+public:
+    RelaxedCapture() { cudaThreadExchangeStreamCaptureMode(&mode_); }
+    ~RelaxedCapture() { cudaThreadExchangeStreamCaptureMode(&mode_); }
+    RelaxedCapture(const RelaxedCapture &) = delete;
+    RelaxedCapture &operator=(const RelaxedCapture &) = delete;
+
+private:
+    cudaStreamCaptureMode mode_ = cudaStreamCaptureModeRelaxed;
+};
+
 std::mutex g_sm_mu;
 int g_sm_count[kMaxDevices] = {};
 
@@ -63,6 +80,7 @@ int64_t current_sm_count()
         return 0;
     std::lock_guard<std::mutex> lk(g_sm_mu);
     if (!g_sm_count[device]) {
+        RelaxedCapture relaxed;
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
             return 0;
@@ -232,6 +250,7 @@ cudaError_t configure(const void *fn, int device)
     for (const FnConfig &c : g_cfg)
         if (c.fn == fn && c.device == device)
             return cudaSuccess;
+    RelaxedCapture relaxed;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSliceMax));
     if (e != cudaSuccess)
@@ -260,6 +279,7 @@ cudaError_t pool_for(int device, cudaMemPool_t *out)
         return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_pool_mu);
     if (!g_pool[device]) {
+        RelaxedCapture relaxed;
         cudaMemPoolProps props = {};
         props.allocType = cudaMemAllocationTypePinned;
         props.location.type = cudaMemLocationTypeDevice;
@@ -349,6 +369,7 @@ cudaError_t resident_clusters(KernelFn fn, const Plan &p, int device, int64_t *o
                 return cudaSuccess;
             }
     }
+    RelaxedCapture relaxed;
     int n = 0;
     cudaError_t e;
     if (p.C == 1) {
@@ -1095,6 +1116,7 @@ cudaError_t noalloc_scratch(int device, void **out)
 {
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_addr[device]) {
+        RelaxedCapture relaxed;
         void *p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess)

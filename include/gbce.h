@@ -190,7 +190,7 @@ GBCE_API int scale_rows(void *x, int64_t stride, int64_t M, int64_t N, int dtype
  *     calls whose work overlaps on the GPU (on different streams, or from
  *     different host threads) race on it and must be serialised by the caller;
  *   - the first call on each device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     that device current); it may be a call captured into a CUDA graph.
  */
 GBCE_API int ce_fwd_bwd_noalloc(void *logits, int64_t stride, const int64_t *targets, float *loss,
                                 int64_t M, int64_t V, int64_t ignore_index, int dtype,

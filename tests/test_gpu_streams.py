@@ -272,3 +272,65 @@ def test_first_use_from_several_host_threads():
     r = subprocess.run([sys.executable, "-c", _THREADS_CHILD], cwd=root, env=env,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and r.stdout.startswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
+_CAPTURE_FIRST_CHILD = r'''
+import sys
+import torch
+import cross_entropy_loss_ce_gb300 as gbce
+
+II = -100
+torch.zeros(1, device="cuda")
+g = torch.Generator(device="cuda").manual_seed(5)
+x1 = torch.randn((4, 128256), generator=g, device="cuda").to(torch.bfloat16)   # small batch
+x2 = torch.randn((300, 65537), generator=g, device="cuda").to(torch.bfloat16)  # ring
+x3 = torch.randn((64, 3000), generator=g, device="cuda")                       # resident
+t1 = torch.randint(0, 128256, (4,), generator=g, device="cuda")
+t2 = torch.randint(0, 65537, (300,), generator=g, device="cuda")
+x4 = torch.randn((96, 32000), generator=g, device="cuda").to(torch.bfloat16)   # no-alloc call
+t4 = torch.randint(0, 32000, (96,), generator=g, device="cuda")
+a1, a2, a3, a4 = x1.clone(), x2.clone(), torch.empty_like(x3), x4.clone()
+l1, l2, l4 = (torch.empty((), device="cuda") for _ in range(3))
+torch.cuda.synchronize()
+graph = torch.cuda.CUDAGraph()
+# the library's first calls in this process happen inside the capture
+with torch.cuda.graph(graph):
+    gbce.ce_fwd_bwd(a1, t1, II, l1)
+    gbce.ce_fwd_bwd(a2, t2, II, l2)
+    gbce.softmax_fwd(x3, a3)
+    gbce.ce_fwd_bwd_noalloc(a4, t4, II, l4)
+for _ in range(2):
+    a1.copy_(x1); a2.copy_(x2); a4.copy_(x4)
+    graph.replay()
+    torch.cuda.synchronize()
+assert gbce.last_error() == gbce.OK
+b1, b2, b4 = x1.clone(), x2.clone(), x4.clone()
+m1, m2 = gbce.ce_fwd_bwd(b1, t1, II), gbce.ce_fwd_bwd(b2, t2, II)
+m4 = gbce.ce_fwd_bwd(b4, t4, II)
+b3 = gbce.softmax_fwd(x3)
+torch.cuda.synchronize()
+ok = (torch.equal(a1.view(torch.int16), b1.view(torch.int16)) and
+      torch.equal(a2.view(torch.int16), b2.view(torch.int16)) and torch.equal(a3, b3) and
+      torch.equal(a4.view(torch.int16), b4.view(torch.int16)) and
+      float(l1) == float(m1) and float(l2) == float(m2) and float(l4) == float(m4))
+print("ok" if ok else "FAIL mismatch")
+sys.exit(0 if ok else 1)
+'''
+
+
+def test_first_calls_inside_a_graph_capture():
+    """In a fresh process, the library's very first calls are made inside a
+    CUDA graph capture: library load, plans (a small-batch cluster search
+    included), kernel configuration, occupancy queries, the scratch pool and
+    the allocation-free call's static array all happen during capture (in
+    the default, global capture mode); replays equal later direct calls bit
+    for bit."""
+    require_gpu()
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    r = subprocess.run([sys.executable, "-c", _CAPTURE_FIRST_CHILD], cwd=root, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), r.stdout[-2000:] + r.stderr[-3000:]
