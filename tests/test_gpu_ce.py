@@ -224,17 +224,20 @@ def test_other_negative_ignore_index():
     check_grad(xd[keep], ref["grad"][keep], ref["n"], torch.float32, "ignore_index=-1")
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=str)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16], ids=str)
 # 6 rows: warp, resident, the ring on one CTA (unaligned fp32 rows of 48 KB), the ring on a
 # cluster (unaligned rows; a small batch), the ring on a cluster
 @pytest.mark.parametrize("V", [1000, 8000, 12001, 100003, 262147])
 @pytest.mark.parametrize("offset", [50.0, -150.0, 150.0, 1e4, -1e4, 1e6, -1e6])
 def test_ce_large_logits(dtype, V, offset):
-    """Logits far from zero, row maxima up to 2e6 in magnitude, in every kernel
-    regime, within the same tolerances as logits near zero: exp(x - m) is formed
-    from the difference x - m, whose rounding follows |x - m| and not |m|, and
-    the row loss from m - x_y.  Rows with different offsets, one of them ignored."""
+    """Logits far from zero, row maxima up to 2e6 in magnitude (2e4 for fp16,
+    whose range ends at 65504), in every kernel regime, within the same
+    tolerances as logits near zero: exp(x - m) is formed from the difference
+    x - m, whose rounding follows |x - m| and not |m|, and the row loss from
+    m - x_y.  Rows with different offsets, one of them ignored."""
     require_gpu()
+    if dtype == torch.float16 and abs(offset) > 1e4:
+        pytest.skip("beyond the fp16 range")
     M = 6
     g = torch.Generator().manual_seed(V)
     x = torch.randn((M, V), generator=g) * 4

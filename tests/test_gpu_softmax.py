@@ -155,3 +155,25 @@ def test_softmax_masked_rows(dtype, N, M):
     dx = gbce.softmax_bwd(y, dy.cuda())
     assert gbce.last_error() == gbce.OK
     check_softmax_bwd(dx, ref_dx, yh, dy, dtype, f"masked softmax backward {M}x{N}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=str)
+@pytest.mark.parametrize("N", [1000, 4096, 12001, 16384, 100003, 300001])
+@pytest.mark.parametrize("offset", [150.0, -150.0, 1e4, -1e4])
+def test_softmax_large_inputs_16bit(dtype, N, offset):
+    """bf16 and fp16 rows far from zero (row maxima up to 2e4) in every regime,
+    forward and backward against the oracle at the 16-bit tolerances."""
+    require_gpu()
+    g = torch.Generator().manual_seed(N)
+    x = torch.randn((4, N), generator=g) * 4
+    x += torch.tensor([offset, -offset, 0.5 * offset, 2 * offset])[:, None]
+    x = x.to(dtype)
+    y = gbce.softmax_fwd(x.cuda())
+    assert gbce.last_error() == gbce.OK
+    check_softmax(y, oracle.softmax_fwd(host(x)), dtype, f"N={N} offset={offset}")
+    yh = y.cpu()
+    dy = (torch.randn((4, N), generator=g) * 3).to(dtype)
+    dx = gbce.softmax_bwd(y, dy.cuda())
+    assert gbce.last_error() == gbce.OK
+    check_softmax_bwd(dx, oracle.softmax_bwd(host(yh), host(dy)), yh, dy, dtype,
+                      f"backward N={N} offset={offset}")
