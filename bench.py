@@ -48,6 +48,7 @@ DEFAULT_WORKLOAD = "ce_bf16_16384x128256"
 # the large-vocabulary CE workloads held to >= 80% of the measured copy bandwidth
 GATED_CE = ("ce_bf16_8192x32000", "ce_bf16_16384x128256", "ce_f32_4096x250007")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # HBM3e nominal bandwidth of a GB300, reported beside the measured peak
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "cross_entropy_loss_ce_gb300", "csrc", f)
@@ -586,7 +587,8 @@ def run_gbce(args, ws, rank, local):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                 "kernel": gbce.plan("ce", w.M, w.V, w.dtype)[0] + "<CE>", "kernel_ms": kavg_ms,
-                "algorithmic_bytes": alg, "peak_kind": f"{peak_kind} (hbm_gbs, burst)"}
+                "algorithmic_bytes": alg, "peak_kind": f"{peak_kind} (hbm_gbs, burst)",
+                "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS}
 
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
