@@ -49,6 +49,7 @@ DEFAULT_WORKLOAD = "ce_bf16_16384x128256"
 GATED_CE = ("ce_bf16_8192x32000", "ce_bf16_16384x128256", "ce_f32_4096x250007")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # HBM3e nominal bandwidth of a GB300, reported beside the measured peak
+E2E_STEPS = 20  # timed end-to-end steps (each moves 4.2 GB over the host link)
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "cross_entropy_loss_ce_gb300", "csrc", f)
@@ -363,17 +364,17 @@ def time_ce_e2e(w, x_pinned, t_pinned, steps, ws):
     grad = torch.empty(x_pinned.shape, dtype=x_pinned.dtype, device="cuda")
     loss_host = torch.empty((), dtype=torch.float32).pin_memory()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    total = 0.0
+    step_ms = []
     for i in range(steps + 1):
         barrier_sync(ws)
         start.record()
         gbce.ce_fwd_bwd_host(x_pinned, t_pinned, workloads.IGNORE_INDEX, grad, loss_host)
         stop.record()
         barrier_sync(ws)
-        if i > 0:  # the first iteration is a warm-up
-            total += start.elapsed_time(stop)
+        if i > 0:  # the first iteration is a warm-up (the library's one-time set-up)
+            step_ms.append(start.elapsed_time(stop))
     h2d = x_pinned.numel() * x_pinned.element_size() + t_pinned.numel() * 8
-    return total, h2d, 4
+    return sum(step_ms), h2d, 4, sorted(step_ms)
 
 
 def host_link_gbs(x_pinned, reps: int = 3) -> float:
@@ -613,13 +614,20 @@ def run_gbce(args, ws, rank, local):
         # measurably slow this process's later host-to-device copies
         x_pinned = xd0.cpu().pin_memory()
         t_pinned = td.cpu().pin_memory()
-        e2e_ms, h2d, d2h = time_ce_e2e(w, x_pinned, t_pinned, min(args.steps, 10), ws)
+        e2e_steps = min(args.steps, E2E_STEPS)
+        link_before = host_link_gbs(x_pinned)
+        e2e_ms, h2d, d2h, step_ms = time_ce_e2e(w, x_pinned, t_pinned, e2e_steps, ws)
+        link_after = host_link_gbs(x_pinned)
         e2e_ms = max_over_ranks(e2e_ms, ws)
-        e2e_steps = min(args.steps, 10)
+        # the value is the mean over the steps; the spread and the link measured
+        # on either side show a step slowed by other traffic on the host link
         line["e2e"] = {"value": sum_over_ranks(float(w.M * e2e_steps), ws) / (e2e_ms / 1e3),
                        "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e2e_ms / e2e_steps,
-                       "host_link_h2d_gbs": host_link_gbs(x_pinned)}
+                       "ms_per_step_median": step_ms[len(step_ms) // 2],
+                       "ms_per_step_min": step_ms[0], "ms_per_step_max": step_ms[-1],
+                       "host_link_h2d_gbs": min(link_before, link_after),
+                       "host_link_h2d_gbs_before_after": [link_before, link_after]}
         del x_pinned
 
     if not args.no_workloads:
