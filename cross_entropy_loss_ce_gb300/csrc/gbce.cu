@@ -60,13 +60,18 @@ size_t elem_size(int dtype) { return dtype == GBCE_F32 ? 4 : 2; }
 // allows them, and the thread's mode is restored after.
 class RelaxedCapture {
 public:
-    RelaxedCapture() { cudaThreadExchangeStreamCaptureMode(&mode_); }
-    ~RelaxedCapture() { cudaThreadExchangeStreamCaptureMode(&mode_); }
+    RelaxedCapture() : switched_(cudaThreadExchangeStreamCaptureMode(&mode_) == cudaSuccess) {}
+    ~RelaxedCapture()
+    {
+        if (switched_)  // give the thread back the mode it had
+            cudaThreadExchangeStreamCaptureMode(&mode_);
+    }
     RelaxedCapture(const RelaxedCapture &) = delete;
     RelaxedCapture &operator=(const RelaxedCapture &) = delete;
 
 private:
     cudaStreamCaptureMode mode_ = cudaStreamCaptureModeRelaxed;
+    bool switched_;
 };
 
 std::mutex g_sm_mu;
