@@ -42,6 +42,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ce_fwd_bwd.argtypes = [p, i64, p, p, i64, i64, i64, ci, p]
         lib.softmax_fwd.argtypes = [p, i64, p, i64, i64, i64, ci, p]
         lib.softmax_bwd.argtypes = [p, i64, p, i64, p, i64, i64, i64, ci, p]
+        lib.softmax_fwd_ex.argtypes = [p, i64, p, i64, i64, i64, ci, p, p]
+        lib.softmax_bwd_ex.argtypes = [p, i64, p, i64, p, i64, i64, i64, ci, p, p]
         lib.ce_fwd_bwd_ex.argtypes = [p, i64, p, p, p, p, i64, i64, i64, ci, ci, p]
         lib.scale_rows.argtypes = [p, i64, i64, i64, ci, p, ci, p]
         lib.gbce_plan.argtypes = [ci, i64, i64, ci, ci, ctypes.POINTER(ci)]
@@ -272,18 +274,36 @@ class CrossEntropyLoss(torch.nn.Module):
         return cross_entropy(logits, targets, self.ignore_index, self.reduction, self.inplace)
 
 
+def _status_word(status, name="status"):
+    """Device address of a per-call status word: a CUDA int32 tensor of one element."""
+    if status is None:
+        return None
+    if not status.is_cuda or status.dtype != torch.int32 or status.numel() != 1:
+        raise ValueError(f"{name} must be a one-element int32 CUDA tensor")
+    return status.data_ptr()
+
+
 def softmax_fwd(x: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.Tensor:
     """Row softmax of ``x`` [M, N] into ``y`` (allocated when None; may be ``x``)."""
+    return softmax_fwd_ex(x, y, None, stream)
+
+
+def softmax_fwd_ex(x: torch.Tensor, y: torch.Tensor = None, status: torch.Tensor = None,
+                   stream=None) -> torch.Tensor:
+    """softmax_fwd with a status word of the call's own: ``status`` (a one-element
+    int32 CUDA tensor the caller cleared) gets bit 0 set when one of the call's
+    bounded waits gave up."""
     if y is None:
         y = torch.empty_like(x, memory_format=torch.contiguous_format)
     xp, xs, M, N = _matrix(x, "x")
     yp, ys, My, Ny = _matrix(y, "y")
     if (My, Ny) != (M, N) or y.dtype != x.dtype:
         raise ValueError("y must match x in shape and dtype")
-    dev = _call_device(("x", x), ("y", y))
+    sp = _status_word(status)
+    dev = _call_device(("x", x), ("y", y), ("status", status))
     with _OnDevice(dev):
-        rc = load_library().softmax_fwd(xp, xs, yp, ys, M, N, DTYPES[x.dtype],
-                                        _stream_handle(stream, dev))
+        rc = load_library().softmax_fwd_ex(xp, xs, yp, ys, M, N, DTYPES[x.dtype], sp,
+                                           _stream_handle(stream, dev))
     _check(rc, "softmax_fwd")
     return y
 
@@ -291,6 +311,12 @@ def softmax_fwd(x: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.T
 def softmax_bwd(y: torch.Tensor, dy: torch.Tensor, dx: torch.Tensor = None,
                 stream=None) -> torch.Tensor:
     """dx = y * (dy - sum(y * dy, row)) for [M, N] operands (dx may be ``dy``)."""
+    return softmax_bwd_ex(y, dy, dx, None, stream)
+
+
+def softmax_bwd_ex(y: torch.Tensor, dy: torch.Tensor, dx: torch.Tensor = None,
+                   status: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """softmax_bwd with a status word of the call's own (as softmax_fwd_ex)."""
     if dx is None:
         dx = torch.empty_like(dy, memory_format=torch.contiguous_format)
     yp, ys, M, N = _matrix(y, "y")
@@ -298,10 +324,11 @@ def softmax_bwd(y: torch.Tensor, dy: torch.Tensor, dx: torch.Tensor = None,
     xp, xs, Mx, Nx = _matrix(dx, "dx")
     if (Md, Nd) != (M, N) or (Mx, Nx) != (M, N) or not (y.dtype == dy.dtype == dx.dtype):
         raise ValueError("y, dy and dx must share shape and dtype")
-    dev = _call_device(("y", y), ("dy", dy), ("dx", dx))
+    sp = _status_word(status)
+    dev = _call_device(("y", y), ("dy", dy), ("dx", dx), ("status", status))
     with _OnDevice(dev):
-        rc = load_library().softmax_bwd(yp, ys, dp, ds, xp, xs, M, N, DTYPES[y.dtype],
-                                        _stream_handle(stream, dev))
+        rc = load_library().softmax_bwd_ex(yp, ys, dp, ds, xp, xs, M, N, DTYPES[y.dtype], sp,
+                                           _stream_handle(stream, dev))
     _check(rc, "softmax_bwd")
     return dx
 

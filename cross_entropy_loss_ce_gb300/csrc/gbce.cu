@@ -906,14 +906,17 @@ extern "C" int scale_rows(void *x, int64_t stride, int64_t M, int64_t N, int dty
     return map_error(cudaGetLastError());
 }
 
-extern "C" int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_stride, int64_t M,
-                           int64_t N, int dtype, gbce_stream_t stream_)
+extern "C" int softmax_fwd_ex(const void *x, int64_t x_stride, void *y, int64_t y_stride,
+                              int64_t M, int64_t N, int dtype, unsigned int *status,
+                              gbce_stream_t stream_)
 {
     int st = check_common(M, N, dtype);
     if (st)
         return st;
     if ((st = check_matrix(x, x_stride, M, N, dtype)) || (st = check_matrix(y, y_stride, M, N, dtype)))
         return st;
+    if (!aligned_to(status, alignof(unsigned int)))
+        return GBCE_ERR_ALIGN;
     if (M == 0)
         return GBCE_OK;
     const size_t es = elem_size(dtype);
@@ -927,6 +930,7 @@ extern "C" int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_s
     a.so = y_stride;
     a.M = M;
     a.cols = N;
+    a.fail = status;
     a.C = p.C;
     a.per_vec = p.per_vec;
     a.chunk_vec = p.chunk_vec;
@@ -935,9 +939,15 @@ extern "C" int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_s
                                  reinterpret_cast<cudaStream_t>(stream_)));
 }
 
-extern "C" int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int64_t dy_stride,
-                           void *dx, int64_t dx_stride, int64_t M, int64_t N, int dtype,
-                           gbce_stream_t stream_)
+extern "C" int softmax_fwd(const void *x, int64_t x_stride, void *y, int64_t y_stride, int64_t M,
+                           int64_t N, int dtype, gbce_stream_t stream)
+{
+    return softmax_fwd_ex(x, x_stride, y, y_stride, M, N, dtype, nullptr, stream);
+}
+
+extern "C" int softmax_bwd_ex(const void *y, int64_t y_stride, const void *dy, int64_t dy_stride,
+                              void *dx, int64_t dx_stride, int64_t M, int64_t N, int dtype,
+                              unsigned int *status, gbce_stream_t stream_)
 {
     int st = check_common(M, N, dtype);
     if (st)
@@ -946,6 +956,8 @@ extern "C" int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int6
         (st = check_matrix(dy, dy_stride, M, N, dtype)) ||
         (st = check_matrix(dx, dx_stride, M, N, dtype)))
         return st;
+    if (!aligned_to(status, alignof(unsigned int)))
+        return GBCE_ERR_ALIGN;
     if (M == 0)
         return GBCE_OK;
     const size_t es = elem_size(dtype);
@@ -961,12 +973,20 @@ extern "C" int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int6
     a.so = dx_stride;
     a.M = M;
     a.cols = N;
+    a.fail = status;
     a.C = p.C;
     a.per_vec = p.per_vec;
     a.chunk_vec = p.chunk_vec;
     a.nslot = p.nslot;
     return map_error(launch_rows(pick<Op::SoftmaxBwd>(dtype, p), p, a,
                                  reinterpret_cast<cudaStream_t>(stream_)));
+}
+
+extern "C" int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int64_t dy_stride,
+                           void *dx, int64_t dx_stride, int64_t M, int64_t N, int dtype,
+                           gbce_stream_t stream)
+{
+    return softmax_bwd_ex(y, y_stride, dy, dy_stride, dx, dx_stride, M, N, dtype, nullptr, stream);
 }
 
 extern "C" const char *gbce_plan(int op, int64_t M, int64_t cols, int dtype, int same_phase,

@@ -249,6 +249,30 @@ GBCE_API int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int64_
                 int64_t dx_stride, int64_t M, int64_t N, int dtype, gbce_stream_t stream);
 
 /*
+ * softmax_fwd_ex, softmax_bwd_ex -- softmax_fwd and softmax_bwd with a status
+ * word of the call's own.
+ *
+ * Defined by: as softmax_fwd and softmax_bwd.  The pages' kernels have no
+ * failure path; the status word lets a caller with concurrent calls (several
+ * streams or host threads) tell which call failed, where the device flags of
+ * gbce_last_error belong to the whole device.
+ *
+ *   status  NULL (the same as softmax_fwd / softmax_bwd), or one caller-owned
+ *           device unsigned int, 4-byte aligned (else GBCE_ERR_ALIGN before any
+ *           launch), that the caller clears before the call.  The call ORs
+ *           bit 0 (1u) into it when one of its bounded waits gave up, i.e. when
+ *           it also raises GBCE_ERR_TIMEOUT in the device flags; it writes
+ *           nothing else there.  Read it after the call's work on `stream`
+ *           has completed.  Other arguments, results and errors: as for
+ *           softmax_fwd / softmax_bwd.
+ */
+GBCE_API int softmax_fwd_ex(const void *x, int64_t x_stride, void *y, int64_t y_stride, int64_t M,
+                            int64_t N, int dtype, unsigned int *status, gbce_stream_t stream);
+GBCE_API int softmax_bwd_ex(const void *y, int64_t y_stride, const void *dy, int64_t dy_stride,
+                            void *dx, int64_t dx_stride, int64_t M, int64_t N, int dtype,
+                            unsigned int *status, gbce_stream_t stream);
+
+/*
  * softmax_bwd_bsr -- block-sparse softmax backward through a look-up table,
  * dx = y * (dy - sum(y * dy)) * scale over every row of a block-sparse matrix.
  *

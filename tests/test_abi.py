@@ -27,6 +27,8 @@ def lib():
     lib.ce_fwd_bwd.argtypes = [p, i64, p, p, i64, i64, i64, ci, p]
     lib.softmax_fwd.argtypes = [p, i64, p, i64, i64, i64, ci, p]
     lib.softmax_bwd.argtypes = [p, i64, p, i64, p, i64, i64, i64, ci, p]
+    lib.softmax_fwd_ex.argtypes = [p, i64, p, i64, i64, i64, ci, p, p]
+    lib.softmax_bwd_ex.argtypes = [p, i64, p, i64, p, i64, i64, i64, ci, p, p]
     lib.ce_fwd_bwd_ex.argtypes = [p, i64, p, p, p, p, i64, i64, i64, ci, ci, p]
     lib.scale_rows.argtypes = [p, i64, i64, i64, ci, p, ci, p]
     lib.gbce_status_string.restype = ctypes.c_char_p
@@ -42,7 +44,8 @@ def test_header_declares_the_boundary():
     assert {"ce_fwd_bwd", "softmax_fwd", "softmax_bwd", "gbce_last_error",
             "gbce_status_string", "gbce_timing_enable", "gbce_timing_read", "ce_fwd_bwd_ex",
             "scale_rows", "softmax_bwd_bsr", "gbce_bsr_plan", "ce_fwd_bwd_noalloc",
-            "ce_fwd_bwd_host", "gbce_pool_reserved", "gbce_test_failure_path"} <= names
+            "ce_fwd_bwd_host", "gbce_pool_reserved", "gbce_test_failure_path",
+            "softmax_fwd_ex", "softmax_bwd_ex"} <= names
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -109,6 +112,17 @@ def test_softmax_fwd_rejects_bad_arguments(lib, args, code):
 ])
 def test_softmax_bwd_rejects_bad_arguments(lib, args, code):
     assert lib.softmax_bwd(*args, None) == code
+
+
+def test_softmax_ex_checks_its_status_word(lib):
+    # the _ex forms take the same arguments plus a status word: checked like
+    # the others, and a word off its 4-byte alignment is rejected before any launch
+    assert lib.softmax_fwd_ex(None, 8, FAKE, 8, 2, 8, 0, None, None) == 1
+    assert lib.softmax_fwd_ex(FAKE, 8, FAKE, 8, 2, 8, 0, FAKE + 2, None) == 4
+    assert lib.softmax_bwd_ex(FAKE, 8, FAKE, 8, FAKE, 8, 2, 8, 0, FAKE + 1, None) == 4
+    assert lib.softmax_bwd_ex(FAKE, 6, FAKE, 8, FAKE, 8, 2, 8, 0, FAKE, None) == 2
+    assert lib.softmax_fwd_ex(None, 8, None, 8, 0, 8, 0, FAKE, None) == 0  # M = 0
+    assert lib.softmax_bwd_ex(None, 8, None, 8, None, 8, 0, 8, 1, FAKE, None) == 0
 
 
 def test_empty_softmax_is_a_noop(lib):

@@ -196,3 +196,37 @@ def test_defaults_after_the_failure_tests():
     assert gbce.last_error() == gbce.OK
     assert math.isfinite(float(loss.item()))
     check_grad(xd[torch.as_tensor(rows, device="cuda")], ref["grad"], ref["n"], w.dtype)
+
+
+def test_status_words_tell_concurrent_calls_apart(failure_path):
+    """softmax_fwd_ex / softmax_bwd_ex: with a copy left out, the staged calls
+    (a ring forward, a resident backward) set bit 0 of their own status words
+    while a warp-kernel call (no bulk copies) on another stream, running at the
+    same time, leaves its word at 0; the device flag reports the timeout for
+    the device.  With every copy issued again, a staged call's word stays 0."""
+    xa, _, _ = workloads.make_softmax_inputs(400, 16384)      # ring, held 64 KB rows
+    _, yb, dyb = workloads.make_softmax_inputs(64, 4096)      # resident backward
+    xc, _, _ = workloads.make_softmax_inputs(64, 1000)        # warp kernel
+    words = torch.zeros(4, dtype=torch.int32, device="cuda")
+    sa, sb, sc = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    xad, ybd, dybd, xcd = xa.cuda(), yb.cuda(), dyb.cuda(), xc.cuda()
+    torch.cuda.synchronize()
+    failure_path(0)
+    gbce.softmax_fwd_ex(xad, status=words[0:1], stream=sa)
+    gbce.softmax_bwd_ex(ybd, dybd, status=words[1:2], stream=sb)
+    yc = gbce.softmax_fwd_ex(xcd, status=words[2:3], stream=sc)
+    torch.cuda.synchronize()
+    assert words.tolist() == [1, 1, 0, 0]
+    assert gbce.last_error() == gbce.ERR_TIMEOUT
+    check_softmax(yc, oracle.softmax_fwd(host(xc)), torch.float32, "the unaffected call")
+
+    failure_path(-1)
+    words.zero_()
+    ya = gbce.softmax_fwd_ex(xad, status=words[0:1])
+    dx = gbce.softmax_bwd_ex(ybd, dybd, status=words[1:2])
+    torch.cuda.synchronize()
+    assert words.tolist() == [0, 0, 0, 0]
+    assert gbce.last_error() == gbce.OK
+    check_softmax(ya, oracle.softmax_fwd(host(xa)), torch.float32, "after the defaults came back")
+    check_softmax_bwd(dx, oracle.softmax_bwd(host(yb), host(dyb)), yb, dyb, torch.float32,
+                      "backward after the defaults came back")

@@ -177,3 +177,18 @@ def test_softmax_large_inputs_16bit(dtype, N, offset):
     assert gbce.last_error() == gbce.OK
     check_softmax_bwd(dx, oracle.softmax_bwd(host(yh), host(dy)), yh, dy, dtype,
                       f"backward N={N} offset={offset}")
+
+
+@pytest.mark.parametrize("N", [1000, 4096, 16384, 300001])
+def test_softmax_ex_equals_the_plain_calls(N):
+    """softmax_fwd_ex / softmax_bwd_ex with a status word: bit-identical to
+    softmax_fwd / softmax_bwd, and the word stays 0."""
+    require_gpu()
+    M = 6 if N > 100000 else 300
+    x, y, dy = workloads.make_softmax_inputs(M, N, device="cuda")
+    words = torch.zeros(2, dtype=torch.int32, device="cuda")
+    assert torch.equal(gbce.softmax_fwd_ex(x, status=words[0:1]), gbce.softmax_fwd(x))
+    assert torch.equal(gbce.softmax_bwd_ex(y, dy, status=words[1:2]), gbce.softmax_bwd(y, dy))
+    assert words.tolist() == [0, 0] and gbce.last_error() == gbce.OK
+    with pytest.raises(ValueError):
+        gbce.softmax_fwd_ex(x, status=torch.zeros(1, dtype=torch.int64, device="cuda"))
