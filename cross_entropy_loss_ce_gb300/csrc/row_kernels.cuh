@@ -897,11 +897,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
         uint32_t slot = 0, ph = 0, xph = 0;
         int live = 0;
         bool ok = true;
-        if constexpr (OP == Op::CE) {
+        if constexpr (OP == Op::CE)
             asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-            wait_prerequisite_grid();  // n comes from the count kernel
-        }
-        const float nf = OP == Op::CE ? static_cast<float>(*a.n_ptr) : 1.f;
+        // n (from the count kernel) is first needed by a row's pass 2: pass 1 of
+        // the first row overlaps the count kernel
+        bool have_n = OP != Op::CE;
+        float nf = 1.f;
         int64_t ynext = (OP == Op::CE && cid < M) ? a.targets[cid] : 0;
         for (int row = cid; row < M; row += G) {
             const int64_t y = ynext;  // loaded one row ahead
@@ -1171,6 +1172,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
             // ---- pass 2: the slice again (the same slots when held, else a
             // second read that L2 serves), chunks in order
             float scale = 0.f, sub = 0.f;
+            if constexpr (OP == Op::CE) {
+                if (!have_n) {
+                    wait_prerequisite_grid();
+                    nf = static_cast<float>(*a.n_ptr);
+                    have_n = true;
+                }
+            }
             if constexpr (OP != Op::SoftmaxBwd) {
                 if constexpr (OP == Op::CE)
                     ce_row_factor(a, row, r.y, nf, scale, sub);
@@ -1296,6 +1304,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rows_ring_kernel(const RowA
                         a.row_loss[row] = __int_as_float(0x7fc00000);
                 }
             }
+        }
+        if constexpr (OP == Op::CE) {
+            if (!have_n)  // the count kernel has cleared the failure word; see ce_row_exit_order
+                wait_prerequisite_grid();
         }
         if (!ok && lane == 0)  // this warp gave up (perhaps in a last pass 2 no row vote saw)
             raise_timeout(a.fail);
