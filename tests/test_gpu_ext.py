@@ -151,3 +151,36 @@ def test_softmax_fp16(N):
     check_softmax(gbce.softmax_fwd(x.cuda()), ref_y, torch.float16, f"fp16 softmax N={N}")
     check_softmax_bwd(gbce.softmax_bwd(y.cuda(), dy.cuda()), ref_dx, y, dy, torch.float16,
                       f"fp16 softmax bwd N={N}")
+
+
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_autograd_under_torch_compile(reduction):
+    """The autograd form inside torch.compile: dynamo breaks the graph at the
+    library call (a foreign function) and runs it eagerly, in place, so the
+    loss and gradients match the eager run."""
+    require_gpu()
+    torch.manual_seed(3)
+    M, H, V = 256, 256, 32000
+    head = torch.nn.Linear(H, V, bias=False).cuda().to(torch.bfloat16)
+    loss_fn = gbce.CrossEntropyLoss(reduction=reduction)
+    h = torch.randn(M, H, device="cuda", dtype=torch.bfloat16, requires_grad=True)
+    t = torch.randint(0, V, (M,), device="cuda")
+    t[::9] = II
+    w_out = torch.randn(M, device="cuda") if reduction == "none" else None
+
+    def step(h, t):
+        loss = loss_fn(head(h), t)
+        return (loss * w_out).sum() if reduction == "none" else loss
+
+    results = []
+    for f in (step, torch.compile(step)):
+        head.weight.grad, h.grad = None, None
+        loss = f(h, t)
+        loss.backward()
+        torch.cuda.synchronize()
+        results.append((loss.detach().float(), h.grad.float(), head.weight.grad.float()))
+    assert gbce.last_error() == gbce.OK
+    (le, he, we), (lc, hc, wc) = results
+    assert torch.allclose(lc, le, rtol=1e-3, atol=1e-5), (lc, le)
+    for got, ref in ((hc, he), (wc, we)):
+        assert torch.allclose(got, ref, rtol=2e-2, atol=2e-2 * ref.abs().max().item())
