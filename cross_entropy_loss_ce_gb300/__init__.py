@@ -20,6 +20,8 @@ REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 OK, ERR_NULL, ERR_SIZE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA, ERR_BAD_TARGET, ERR_TIMEOUT, \
     ERR_NO_DEVICE, ERR_REDUCTION, ERR_BAD_TABLE = range(11)
+# bits a call ORs into its own status word (gbce_status_bit)
+STATUS_TIMEOUT, STATUS_BAD_TABLE = 1, 2
 
 _lib = None
 
@@ -54,6 +56,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gbce_timing_enable.argtypes = [ci]
         lib.softmax_bwd_bsr.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, i64, i64,
                                         ctypes.c_float, ci, p]
+        lib.softmax_bwd_bsr_ex.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, i64, i64,
+                                           ctypes.c_float, ci, p, p]
         lib.gbce_bsr_plan.argtypes = [i64, i64, ci, ci, ctypes.POINTER(ci)]
         lib.gbce_bsr_plan.restype = ctypes.c_char_p
         lib.gbce_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
@@ -291,8 +295,8 @@ def softmax_fwd(x: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.T
 def softmax_fwd_ex(x: torch.Tensor, y: torch.Tensor = None, status: torch.Tensor = None,
                    stream=None) -> torch.Tensor:
     """softmax_fwd with a status word of the call's own: ``status`` (a one-element
-    int32 CUDA tensor the caller cleared) gets bit 0 set when one of the call's
-    bounded waits gave up."""
+    int32 CUDA tensor the caller cleared) gets STATUS_TIMEOUT when one of the
+    call's bounded waits gave up."""
     if y is None:
         y = torch.empty_like(x, memory_format=torch.contiguous_format)
     xp, xs, M, N = _matrix(x, "x")
@@ -344,6 +348,17 @@ def softmax_bwd_bsr(y: torch.Tensor, dy: torch.Tensor, lut: torch.Tensor, n_bloc
     defaults to ``dy`` (in place, as the page's kernel stores); only the
     positions the table names are written.
     """
+    return softmax_bwd_bsr_ex(y, dy, lut, n_block_rows, nblocks, block, sizemax, scale, dx,
+                              None, stream)
+
+
+def softmax_bwd_bsr_ex(y: torch.Tensor, dy: torch.Tensor, lut: torch.Tensor, n_block_rows: int,
+                       nblocks: int, block: int, sizemax: int, scale: float = 1.0,
+                       dx: torch.Tensor = None, status: torch.Tensor = None,
+                       stream=None) -> torch.Tensor:
+    """softmax_bwd_bsr with a status word of the call's own: ``status`` (a
+    one-element int32 CUDA tensor the caller cleared) gets STATUS_BAD_TABLE when
+    the call finds a malformed table entry."""
     if dx is None:
         dx = dy
     yp, ys, Z, Ly = _matrix(y, "y")
@@ -355,12 +370,13 @@ def softmax_bwd_bsr(y: torch.Tensor, dy: torch.Tensor, lut: torch.Tensor, n_bloc
         raise ValueError("y, dy and dx must hold nblocks * block^2 elements per batch item")
     if lut.dtype != torch.int32 or lut.dim() != 1 or not lut.is_cuda or not lut.is_contiguous():
         raise ValueError("lut must be a contiguous 1-D int32 CUDA tensor")
-    dev = _call_device(("y", y), ("dy", dy), ("dx", dx), ("lut", lut))
+    sp = _status_word(status)
+    dev = _call_device(("y", y), ("dy", dy), ("dx", dx), ("lut", lut), ("status", status))
     with _OnDevice(dev):
-        rc = load_library().softmax_bwd_bsr(yp, ys, dp, ds, xp, xs, lut.data_ptr(), lut.numel(),
-                                            n_block_rows, nblocks, block, sizemax, Z,
-                                            float(scale), DTYPES[y.dtype],
-                                            _stream_handle(stream, dev))
+        rc = load_library().softmax_bwd_bsr_ex(yp, ys, dp, ds, xp, xs, lut.data_ptr(), lut.numel(),
+                                               n_block_rows, nblocks, block, sizemax, Z,
+                                               float(scale), DTYPES[y.dtype], sp,
+                                               _stream_handle(stream, dev))
     _check(rc, "softmax_bwd_bsr")
     return dx
 

@@ -23,7 +23,8 @@
 //                            second (the re-read mostly served by L2).
 // Both validate the table before touching any element: a block-row whose size
 // is negative or above sizemax, whose entries run past the table, or that
-// names a block outside [0, nblocks) raises kFlagBadTable and is left alone.
+// names a block outside [0, nblocks) raises kFlagBadTable (and the call's
+// status word, when it has one) and is left alone.
 #pragma once
 
 #include "device.cuh"
@@ -49,7 +50,18 @@ struct BsrArgs {
     int stage_bytes;  // staged: bytes of one stage (y slab, dy slab; multiple of 16)
     int log2_split;   // staged: CTAs per block-row and batch item (2^log2_split), each a share of its slabs
     float scale;
+    unsigned *status; // the call's own status word (NULL: none); kStatusBadTable marks a bad entry
 };
+
+constexpr unsigned kStatusBadTable = 2u;  // GBCE_STATUS_BAD_TABLE
+
+// A malformed table entry: the device flag, and the call's status word when it has one.
+__device__ __forceinline__ void raise_bad_table(const BsrArgs &a)
+{
+    atomicOr(&g_flags, kFlagBadTable);
+    if (a.status)
+        atomicOr(a.status, kStatusBadTable);
+}
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
 {
@@ -142,7 +154,7 @@ __global__ void __launch_bounds__(NT) bsr_bwd_staged_kernel(const BsrArgs a)
         if (lane == 0) {
             s_size = size;
             if (size < 0)
-                atomicOr(&g_flags, kFlagBadTable);
+                raise_bad_table(a);
         }
     }
     __syncthreads();
@@ -310,7 +322,7 @@ __global__ void __launch_bounds__(NT) bsr_bwd_unstaged_kernel(const BsrArgs a)
             s_size = size;
             s_off = off;
             if (size < 0)
-                atomicOr(&g_flags, kFlagBadTable);
+                raise_bad_table(a);
         }
     }
     __syncthreads();

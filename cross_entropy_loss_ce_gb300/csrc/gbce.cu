@@ -13,6 +13,8 @@
 #include "row_kernels.cuh"
 #include "bsr_kernels.cuh"
 
+static_assert(gbce::kStatusBadTable == GBCE_STATUS_BAD_TABLE, "status bits of the ABI");
+
 namespace gbce {
 namespace {
 
@@ -1189,16 +1191,19 @@ extern "C" int ce_fwd_bwd_noalloc(void *logits, int64_t stride, const int64_t *t
     return map_error(e);
 }
 
-extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
-                               int64_t dy_zstride, void *dx, int64_t dx_zstride,
-                               const int32_t *lut, int64_t lut_len, int64_t n_block_rows,
-                               int64_t nblocks, int64_t block, int64_t sizemax, int64_t Z,
-                               float scale, int dtype, gbce_stream_t stream_)
+extern "C" int softmax_bwd_bsr_ex(const void *y, int64_t y_zstride, const void *dy,
+                                  int64_t dy_zstride, void *dx, int64_t dx_zstride,
+                                  const int32_t *lut, int64_t lut_len, int64_t n_block_rows,
+                                  int64_t nblocks, int64_t block, int64_t sizemax, int64_t Z,
+                                  float scale, int dtype, unsigned int *status,
+                                  gbce_stream_t stream_)
 {
     int st = check_bsr_shape(y_zstride, dy_zstride, dx_zstride, lut_len, n_block_rows, nblocks,
                              block, sizemax, Z, dtype);
     if (st)
         return st;
+    if (!aligned_to(status, alignof(unsigned int)))
+        return GBCE_ERR_ALIGN;
     if (Z == 0 || n_block_rows == 0 || sizemax == 0)
         return GBCE_OK;
     if (!y || !dy || !dx || !lut)
@@ -1238,6 +1243,7 @@ extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
     a.sizemax = static_cast<int>(sizemax);
     a.ids_bytes = p.ids_bytes;
     a.scale = scale;
+    a.status = status;
 
     a.stage_bytes = p.stage_bytes;
     a.log2_split = p.log2_split;
@@ -1254,6 +1260,17 @@ extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
     TimedRegion timed(stream);
     fn<<<static_cast<unsigned>(units), kBsrThreads, p.staged ? p.smem : 0, stream>>>(a);
     return map_error(cudaGetLastError());
+}
+
+extern "C" int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy,
+                               int64_t dy_zstride, void *dx, int64_t dx_zstride,
+                               const int32_t *lut, int64_t lut_len, int64_t n_block_rows,
+                               int64_t nblocks, int64_t block, int64_t sizemax, int64_t Z,
+                               float scale, int dtype, gbce_stream_t stream)
+{
+    return softmax_bwd_bsr_ex(y, y_zstride, dy, dy_zstride, dx, dx_zstride, lut, lut_len,
+                              n_block_rows, nblocks, block, sizemax, Z, scale, dtype, nullptr,
+                              stream);
 }
 
 extern "C" const char *gbce_bsr_plan(int64_t block, int64_t sizemax, int dtype, int aligned,

@@ -54,6 +54,12 @@ enum gbce_dtype {
     GBCE_F16 = 2   /* IEEE binary16; arithmetic is fp32, results rounded to nearest even */
 };
 
+/* Bits a call ORs into its own status word (the _ex entry points that take one). */
+enum gbce_status_bit {
+    GBCE_STATUS_TIMEOUT = 1,  /* one of the call's bounded waits gave up (GBCE_ERR_TIMEOUT) */
+    GBCE_STATUS_BAD_TABLE = 2 /* a block-sparse look-up table entry is malformed (GBCE_ERR_BAD_TABLE) */
+};
+
 /* Reductions of ce_fwd_bwd_ex (PyTorch CrossEntropyLoss's reduction argument). */
 enum gbce_reduction {
     GBCE_MEAN = 0, /* L = sum of row losses / n (n = rows whose target is not ignored) */
@@ -260,9 +266,9 @@ GBCE_API int softmax_bwd(const void *y, int64_t y_stride, const void *dy, int64_
  *   status  NULL (the same as softmax_fwd / softmax_bwd), or one caller-owned
  *           device unsigned int, 4-byte aligned (else GBCE_ERR_ALIGN before any
  *           launch), that the caller clears before the call.  The call ORs
- *           bit 0 (1u) into it when one of its bounded waits gave up, i.e. when
- *           it also raises GBCE_ERR_TIMEOUT in the device flags; it writes
- *           nothing else there.  Read it after the call's work on `stream`
+ *           GBCE_STATUS_TIMEOUT into it when one of its bounded waits gave up,
+ *           i.e. when it also raises GBCE_ERR_TIMEOUT in the device flags; it
+ *           writes nothing else there.  Read it after the call's work on `stream`
  *           has completed.  Other arguments, results and errors: as for
  *           softmax_fwd / softmax_bwd.
  */
@@ -311,6 +317,22 @@ GBCE_API int softmax_bwd_bsr(const void *y, int64_t y_zstride, const void *dy, i
                              int64_t n_block_rows, int64_t nblocks, int64_t block,
                              int64_t sizemax, int64_t Z, float scale, int dtype,
                              gbce_stream_t stream);
+
+/*
+ * softmax_bwd_bsr_ex -- softmax_bwd_bsr with a status word of the call's own.
+ *
+ * Defined by: as softmax_bwd_bsr.  status: NULL (the same as softmax_bwd_bsr),
+ * or one caller-owned device unsigned int, 4-byte aligned (else GBCE_ERR_ALIGN
+ * before any launch), cleared by the caller; the call ORs GBCE_STATUS_BAD_TABLE
+ * into it when it finds a malformed table entry (and raises
+ * GBCE_ERR_BAD_TABLE in the device flags), nothing else.  Read it after the
+ * call's work on `stream` has completed.
+ */
+GBCE_API int softmax_bwd_bsr_ex(const void *y, int64_t y_zstride, const void *dy, int64_t dy_zstride,
+                                void *dx, int64_t dx_zstride, const int32_t *lut, int64_t lut_len,
+                                int64_t n_block_rows, int64_t nblocks, int64_t block,
+                                int64_t sizemax, int64_t Z, float scale, int dtype,
+                                unsigned int *status, gbce_stream_t stream);
 
 /*
  * gbce_bsr_plan -- the kernel softmax_bwd_bsr uses for `block`, `sizemax` and

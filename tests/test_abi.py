@@ -34,6 +34,8 @@ def lib():
     lib.gbce_status_string.restype = ctypes.c_char_p
     lib.softmax_bwd_bsr.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, i64, i64,
                                     ctypes.c_float, ci, p]
+    lib.softmax_bwd_bsr_ex.argtypes = [p, i64, p, i64, p, i64, p, i64, i64, i64, i64, i64, i64,
+                                       ctypes.c_float, ci, p, p]
     lib.gbce_bsr_plan.argtypes = [i64, i64, ci, ci, ctypes.POINTER(ci)]
     lib.gbce_bsr_plan.restype = ctypes.c_char_p
     return lib
@@ -45,7 +47,7 @@ def test_header_declares_the_boundary():
             "gbce_status_string", "gbce_timing_enable", "gbce_timing_read", "ce_fwd_bwd_ex",
             "scale_rows", "softmax_bwd_bsr", "gbce_bsr_plan", "ce_fwd_bwd_noalloc",
             "ce_fwd_bwd_host", "gbce_pool_reserved", "gbce_test_failure_path",
-            "softmax_fwd_ex", "softmax_bwd_ex"} <= names
+            "softmax_fwd_ex", "softmax_bwd_ex", "softmax_bwd_bsr_ex"} <= names
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -123,6 +125,11 @@ def test_softmax_ex_checks_its_status_word(lib):
     assert lib.softmax_bwd_ex(FAKE, 6, FAKE, 8, FAKE, 8, 2, 8, 0, FAKE, None) == 2
     assert lib.softmax_fwd_ex(None, 8, None, 8, 0, 8, 0, FAKE, None) == 0  # M = 0
     assert lib.softmax_bwd_ex(None, 8, None, 8, None, 8, 0, 8, 1, FAKE, None) == 0
+    # the block-sparse form: a status word off its alignment, after the shape checks
+    bsr = (FAKE, 64, FAKE, 64, FAKE, 64, FAKE, 6, 1, 4, 4, 1, 1, 1.0, 0)
+    assert lib.softmax_bwd_bsr_ex(*bsr, FAKE + 2, None) == 4
+    assert lib.softmax_bwd_bsr_ex(FAKE, 64, FAKE, 64, FAKE, 64, FAKE, 6, 1, 4, 3, 1, 1, 1.0, 0,
+                                  FAKE, None) == 2  # block 3 is not a power of two
 
 
 def test_empty_softmax_is_a_noop(lib):

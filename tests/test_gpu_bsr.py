@@ -276,3 +276,39 @@ def test_bsr_nothing_to_do():
     gbce.softmax_bwd_bsr(y1, y1, lut0, 1, 1, 4, 1)
     assert bool((y1 == 1).all())
     assert gbce.last_error() == gbce.OK
+
+
+@pytest.mark.parametrize("long_rows", [False, True], ids=["staged", "unstaged"])
+def test_bsr_status_words_tell_calls_apart(long_rows):
+    """softmax_bwd_bsr_ex: a call with a malformed table (a block id out of
+    range) and a call with a good one, on two streams at once, each with its
+    own status word: only the first gets STATUS_BAD_TABLE; the device flag
+    reports the bad table for the device; the good call's result is the
+    plain call's, bit for bit."""
+    require_gpu()
+    block, dtype = 16, torch.float32
+    nb = 1000 if long_rows else 12
+    lay = np.zeros((1, nb, nb), dtype=bool)
+    lay[0, np.arange(nb), np.arange(nb)] = True
+    lay[0, 1, :] = True
+    y, dy, lut, meta, _ = _layout_inputs(lay, block, dtype, 2, 11)
+    nbr, nblocks, sizemax = meta["n_block_rows"], meta["nblocks"], meta["sizemax"]
+    bad_lut = lut.numpy().copy()
+    off = int(bad_lut[2 * 1 + 1])
+    bad_lut[off] = nblocks  # block-row 1's first id: out of range
+    yd, dyd, lutd, badd = y.cuda(), dy.cuda(), lut.cuda(), torch.from_numpy(bad_lut).cuda()
+    words = torch.zeros(2, dtype=torch.int32, device="cuda")
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(sa):
+        gbce.softmax_bwd_bsr_ex(yd, dyd, badd, nbr, nblocks, block, sizemax,
+                                dx=torch.empty_like(dyd), status=words[0:1])
+    with torch.cuda.stream(sb):
+        good = gbce.softmax_bwd_bsr_ex(yd, dyd, lutd, nbr, nblocks, block, sizemax,
+                                       dx=torch.zeros_like(dyd), status=words[1:2])
+    torch.cuda.synchronize()
+    assert words.tolist() == [gbce.STATUS_BAD_TABLE, 0]
+    assert gbce.last_error() == gbce.ERR_BAD_TABLE
+    plain = gbce.softmax_bwd_bsr(yd, dyd, lutd, nbr, nblocks, block, sizemax,
+                                 dx=torch.zeros_like(dyd))
+    assert torch.equal(good, plain) and gbce.last_error() == gbce.OK
