@@ -382,9 +382,11 @@ GBCE_API const char *gbce_plan(int op, int64_t M, int64_t cols, int dtype, int s
  * flag raised by a call still running on another stream may be reported by a
  * later read instead.  A caller that needs a status per call runs its calls
  * on one stream, or synchronises every stream that used the device and calls
- * this once (the result then covers all of those calls).  The cross-entropy
- * calls also carry their own errors in their result: a bad target or a wait
- * that gave up makes the reduced loss NaN.
+ * this once (the result then covers all of those calls), or uses the _ex
+ * entry points, whose status word belongs to the one call (softmax_fwd_ex,
+ * softmax_bwd_ex, softmax_bwd_bsr_ex).  The cross-entropy calls also carry
+ * their own errors in their result: a bad target or a wait that gave up makes
+ * the reduced loss NaN.
  */
 GBCE_API int gbce_last_error(gbce_stream_t stream);
 
