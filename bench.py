@@ -456,7 +456,8 @@ def ce_workload_entry(w, xd0, td, steps, warmup, flush, peak, ws=1):
     lv = float(loss.item())
     if all_ignored != (lv != lv):
         raise RuntimeError(f"{w.name}: unexpected loss {lv}")
-    full = w.M == workloads.CE_WORKLOADS[w.name].M
+    named = workloads.CE_WORKLOADS.get(w.name)
+    full = named is not None and w.M == named.M
     gated = w.name in GATED_CE and full and not all_ignored
     name = w.name if full else f"{w.name} (first {w.M} rows" + (", all ignored)" if all_ignored
                                                                   else ")")
