@@ -1,14 +1,15 @@
 /*
  * The library called from plain C, with nothing but the CUDA runtime: the
  * fused cross-entropy (mean, and with reduction none, per-row losses and a
- * per-row gradient scale), the softmax forward and backward, and the plan
- * query, on inputs read from a file.
+ * per-row gradient scale), the softmax forward and backward (the latter with
+ * a status word of its own), and the plan query, on inputs read from a file.
  *
  *   ce_from_c <in.bin> <out.bin>
  *
  * in.bin:  int64 M, int64 V, then M*V fp32 logits (row-major), M int64 targets,
  *          M*V fp32 upstream gradients dy, M fp32 gradient scales s_r.
  * out.bin: float loss, int32 status of the calls, int32 gbce_last_error,
+ *          int32 status word of the softmax backward call (softmax_bwd_ex),
  *          M*V fp32 gradients of the mean loss, M*V fp32 softmax outputs y,
  *          M*V fp32 softmax backward outputs dx (of y and dy),
  *          M*V fp32 gradients with reduction none scaled by s_r, M fp32 row
@@ -76,14 +77,22 @@ int main(int argc, char **argv)
     /* the softmax of the logits (out of place), its backward in place over dy,
        the fused CE in place (mean), then with reduction none on a second copy */
     int rc = softmax_fwd(d_logits, V, d_soft, V, M, V, GBCE_F32, s);
-    if (rc == GBCE_OK)
-        rc = softmax_bwd(d_soft, V, d_dy, V, d_dy, V, M, V, GBCE_F32, s);
+    unsigned int *d_status = NULL, call_status = 0xffffffffu;
+    if (cudaMalloc((void **)&d_status, sizeof(unsigned int)) != cudaSuccess ||
+        cudaMemset(d_status, 0, sizeof(unsigned int)) != cudaSuccess)
+        return fail("device allocation failed");
+    if (rc == GBCE_OK)  /* with a status word of the call's own */
+        rc = softmax_bwd_ex(d_soft, V, d_dy, V, d_dy, V, M, V, GBCE_F32, d_status, s);
     if (rc == GBCE_OK)
         rc = ce_fwd_bwd(d_logits, V, d_targets, d_loss, M, V, -100, GBCE_F32, s);
     if (rc == GBCE_OK)
         rc = ce_fwd_bwd_ex(d_logits2, V, d_targets, NULL, d_row_loss, d_scale, M, V, -100,
                            GBCE_F32, GBCE_NONE, s);
     const int flags = gbce_last_error(s);
+    if (cudaMemcpy(&call_status, d_status, sizeof(unsigned int), cudaMemcpyDeviceToHost) !=
+        cudaSuccess)
+        return fail("copy from the device failed");
+    cudaFree(d_status);
     if (rc != GBCE_OK)
         fprintf(stderr, "ce_from_c: %s\n", gbce_status_string(rc));
     int ctas = 0;
@@ -97,9 +106,9 @@ int main(int argc, char **argv)
     FILE *o = fopen(argv[2], "wb");
     if (!o)
         return fail("cannot open the output");
-    const int32_t status[2] = {rc, flags};
+    const int32_t status[3] = {rc, flags, (int32_t)call_status};
     int bad = to_host(&loss, d_loss, 4) || fwrite(&loss, 4, 1, o) != 1 ||
-              fwrite(status, 4, 2, o) != 2;
+              fwrite(status, 4, 3, o) != 3;
     const void *blocks[4] = {d_logits, d_soft, d_dy, d_logits2};
     for (int b = 0; b < 4 && !bad; ++b)
         bad = to_host(out, blocks[b], n * 4) || fwrite(out, 4, n, o) != n;

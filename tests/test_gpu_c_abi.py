@@ -1,6 +1,7 @@
 """The library called from a plain C program (GPU): tests/c_abi/ce_from_c.c,
 compiled with gcc against include/gbce.h, libgbce.so and the CUDA runtime (no
-Python or torch in the process), runs softmax_fwd, softmax_bwd (in place),
+Python or torch in the process), runs softmax_fwd, softmax_bwd_ex (in place,
+with a status word of its own),
 ce_fwd_bwd, ce_fwd_bwd_ex (reduction none, per-row scale, row losses) and
 gbce_plan on inputs from a file; its outputs are compared with the oracle on
 the same inputs."""
@@ -52,8 +53,8 @@ def run(exe, tmp_path, x: torch.Tensor, t: torch.Tensor, dy: torch.Tensor, scale
     raw = open(outp, "rb").read()
     n = M * V
     out = dict(loss=float(np.frombuffer(raw[:4], np.float32)[0]),
-               status=list(np.frombuffer(raw[4:12], np.int32)))
-    off = 12
+               status=list(np.frombuffer(raw[4:16], np.int32)))
+    off = 16
     for key in ("grad", "soft", "dx", "grad_none"):
         out[key] = torch.from_numpy(np.frombuffer(raw[off:off + 4 * n], np.float32).reshape(M, V).copy())
         off += 4 * n
@@ -80,7 +81,7 @@ def test_c_program_matches_the_oracle(exe, tmp_path, M, V):
     dy = torch.randn((M, V), generator=g)
     scale = np.random.default_rng(M).standard_normal(M).astype(np.float32)
     out = run(exe, tmp_path, x, t, dy, scale)
-    assert out["status"] == [0, 0]
+    assert out["status"] == [0, 0, 0]  # calls, device flags, the call's status word
     assert (out["plan"], out["ctas"]) == gbce.plan("ce", M, V, torch.float32)
     ref = oracle_ce(x, t)
     what = f"C program {M}x{V}"
