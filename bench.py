@@ -50,6 +50,7 @@ GATED_CE = ("ce_bf16_8192x32000", "ce_bf16_16384x128256", "ce_f32_4096x250007")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # HBM3e nominal bandwidth of a GB300, reported beside the measured peak
 E2E_STEPS = 20  # timed end-to-end steps (each moves 4.2 GB over the host link)
+E2E_WARMUP = 3  # untimed end-to-end steps first (the first carries the one-time set-up)
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "cross_entropy_loss_ce_gb300", "csrc", f)
@@ -365,16 +366,16 @@ def time_ce_e2e(w, x_pinned, t_pinned, steps, ws):
     loss_host = torch.empty((), dtype=torch.float32).pin_memory()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step_ms = []
-    for i in range(steps + 1):
+    for i in range(E2E_WARMUP + steps):
         barrier_sync(ws)
         start.record()
         gbce.ce_fwd_bwd_host(x_pinned, t_pinned, workloads.IGNORE_INDEX, grad, loss_host)
         stop.record()
         barrier_sync(ws)
-        if i > 0:  # the first iteration is a warm-up (the library's one-time set-up)
+        if i >= E2E_WARMUP:
             step_ms.append(start.elapsed_time(stop))
     h2d = x_pinned.numel() * x_pinned.element_size() + t_pinned.numel() * 8
-    return sum(step_ms), h2d, 4, sorted(step_ms)
+    return sum(step_ms), h2d, 4, step_ms
 
 
 def host_link_gbs(x_pinned, reps: int = 3) -> float:
@@ -622,11 +623,13 @@ def run_gbce(args, ws, rank, local):
         e2e_ms = max_over_ranks(e2e_ms, ws)
         # the value is the mean over the steps; the spread and the link measured
         # on either side show a step slowed by other traffic on the host link
+        ordered = sorted(step_ms)
         line["e2e"] = {"value": sum_over_ranks(float(w.M * e2e_steps), ws) / (e2e_ms / 1e3),
                        "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e2e_ms / e2e_steps,
-                       "ms_per_step_median": step_ms[len(step_ms) // 2],
-                       "ms_per_step_min": step_ms[0], "ms_per_step_max": step_ms[-1],
+                       "ms_per_step_median": ordered[len(ordered) // 2],
+                       "ms_per_step_min": ordered[0], "ms_per_step_max": ordered[-1],
+                       "ms_steps": [round(t, 2) for t in step_ms],
                        "host_link_h2d_gbs": min(link_before, link_after),
                        "host_link_h2d_gbs_before_after": [link_before, link_after]}
         del x_pinned
